@@ -1,0 +1,218 @@
+/*
+ * ar.h -- C ABI of the single-GPU R-way all-reduce (sum) and the fused
+ * sum + bias + residual + RMSNorm that follows a row-parallel linear layer.
+ *
+ * The R "rank" partials are R device buffers in the memory of ONE GPU; they
+ * stand in for the peer buffers that the TensorRT-LLM all-reduce reads
+ * through AllReduceParams::peer_comm_buffer_ptrs[MAX_RANKS_PER_NODE]
+ * ("type.d2", AllReduceParams).  There is no second GPU, no NCCL and no
+ * cross-device barrier: the partials are complete when the call is issued
+ * on a stream ordered after their producers.
+ *
+ * Conventions shared by every entry point
+ *   - Return value: an int status (AR_OK or a negative AR_ERR_* code),
+ *     after the plugin's int32 enqueue(..., workspace, stream) noexcept
+ *     ("All Reduce Plugin", IPluginV3OneRuntime::enqueue).  No C++
+ *     exception crosses the ABI.
+ *   - Asynchrony: calls enqueue kernels on `stream` and return at once.
+ *     A launch failure reported by the CUDA runtime maps to AR_ERR_CUDA.
+ *     Argument errors are detected on the host before anything is launched.
+ *   - Memory: every buffer is owned by the caller and lives in device
+ *     memory of the current device.  The `partials` array itself is a HOST
+ *     array of R device pointers; it is read during the call only.  The
+ *     library allocates nothing and keeps no mutable state; calls are
+ *     thread-safe.
+ *   - Layout: tensors are dense and row-major.  The fused call sees
+ *     [tokens, hidden] rows; bias and weight are [hidden]; every tensor of
+ *     one call has the same element type (ar_dtype); eps is a float.
+ *   - Alignment: 16-byte aligned pointers (and, for the fused call, hidden a
+ *     multiple of 16/sizeof(element)) take the 16-byte packed path; anything
+ *     else takes a slower element-wise path.  Misalignment is not an error.
+ *   - Aliasing: out may be one of partials[r] and residual_out may be
+ *     residual (each element is read before it is written).  out and
+ *     residual_out must differ.  Any other overlap is undefined.
+ *   - Empty input (n == 0 or tokens == 0) returns AR_OK and launches nothing.
+ *   - Determinism: the sum of every element is accumulated in fp32 in the
+ *     fixed order partials[0], ..., partials[R-1], bias, residual, and every
+ *     row reduction uses a fixed tree, so results are bit-identical from run
+ *     to run.  residual_out is also bit-identical across strategies.
+ */
+#ifndef TENSOR_ALLREDUCE_RESIDUAL_AR_H
+#define TENSOR_ALLREDUCE_RESIDUAL_AR_H
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t; NULL means the legacy default stream. */
+struct CUstream_st;
+typedef struct CUstream_st* ar_stream_t;
+
+/* Element types.  "type.d2" (PackedOn16Bytes<T>) packs float (4 lanes) and
+ * half (8 lanes) into 16 bytes; bfloat16 (8 lanes) is added beside them. */
+typedef enum { AR_FP32 = 0, AR_FP16 = 1, AR_BF16 = 2 } ar_dtype;
+
+/* Strategy codes: the values of AllReduceStrategyType ("type.d2").
+ * NCCL is recognised but rejected (one GPU, no NCCL). */
+typedef enum { AR_NCCL = 0, AR_ONESHOT = 1, AR_TWOSHOT = 2, AR_AUTO = 3 } ar_strategy;
+
+/* Fusion codes: the values of AllReduceFusionOp ("type.d2"). */
+typedef enum { AR_FUSION_NONE = 0, AR_FUSION_RESIDUAL_RMS_NORM = 1 } ar_fusion_op;
+
+enum {
+    AR_OK = 0,
+    AR_ERR_INVALID_ARG = -1,  /* bad R, NULL required pointer, bad size, eps < 0 ... */
+    AR_ERR_UNSUPPORTED = -2,  /* NCCL strategy, unknown dtype/strategy/fusion, row too long for ONESHOT */
+    AR_ERR_WORKSPACE = -3,    /* TWOSHOT fused without a large enough workspace */
+    AR_ERR_CUDA = -4          /* the CUDA runtime reported an error at launch */
+};
+
+/* MAX_RANKS_PER_NODE ("type.d2", AllReduceParams::peer_comm_buffer_ptrs):
+ * the pages name the bound but not its value. */
+#define AR_MAX_RANKS 16
+
+/* Version of this ABI: major * 10000 + minor * 100 + patch. */
+int ar_version(void);
+
+/* Text for a status code.  Never NULL; the string is static. */
+const char* ar_strerror(int code);
+
+/*
+ * ar_workspace_size -- analogue of getMaxRequiredWorkspaceSize
+ * ("allreduce.d2", common/customAllReduceUtils.h, reached from
+ * selectImplementation and from CustomAllReduceHelper.max_workspace_size_auto).
+ *
+ * Bytes of device workspace that cover ANY fused call of R partials whose
+ * tokens * hidden <= n, with either strategy, rounded up to 256.  The
+ * workspace holds one fp32 partial sum of squares per (row, chunk) of the
+ * two-shot path; the bound is reached by hidden == 1.  Returns 0 when
+ * R < 1, R > AR_MAX_RANKS, n == 0 or dtype is unknown.
+ */
+size_t ar_workspace_size(int R, size_t n, int dtype);
+
+/* Exact workspace bytes for a fused call of this shape (rounded up to 256);
+ * 0 if the shape is invalid. */
+size_t ar_workspace_size_rows(int R, int hidden, int tokens, int dtype);
+
+/*
+ * ar_sum -- out[i] = sum over r of partials[r][i], i < n.
+ * The all-reduce (sum) of the tensor-parallel ranks' partial activations
+ * ("All Reduce Plugin", AllReducePlugin description), computed by the
+ * oneShotAllReduceKernel / twoShotAllReduceKernel routes of
+ * AllReduceDispatch ("allreduce.d2").
+ *
+ *   partials  host array of R device pointers, each to n elements
+ *   R         1 .. AR_MAX_RANKS.  R == 1 is the tpSize == 1 passthrough
+ *             ("All Reduce Plugin": passthrough without tensor parallelism):
+ *             a device copy, or nothing at all when out == partials[0].
+ *   out       device pointer to n elements (may equal one of partials[r])
+ *   n         element count
+ *   dtype     ar_dtype
+ *   strategy  AR_ONESHOT: every block reduces a slice of the whole tensor.
+ *             AR_TWOSHOT: the tensor is cut into R rank slices and block
+ *             group r reduces slice r (the reduce-scatter; the all-gather
+ *             is void on one GPU because the slices land in out directly).
+ *             AR_AUTO: chosen by ar_query_strategy.  Values are
+ *             bit-identical across strategies.
+ * Errors: AR_ERR_INVALID_ARG (R out of range, NULL pointer with n > 0),
+ *         AR_ERR_UNSUPPORTED (AR_NCCL, unknown dtype or strategy),
+ *         AR_ERR_CUDA.
+ */
+int ar_sum(const void* const* partials, int R, void* out, size_t n,
+           int dtype, int strategy, ar_stream_t stream);
+
+/*
+ * ar_residual_rmsnorm -- the RESIDUAL_RMS_NORM fusion (AllReduceFusionOp and
+ * AllReduceFusionParams in "type.d2"; the one-shot
+ * one_shot_all_reduce_norm_kernel -> rms_norm route and the two-shot
+ * twoShotAllReduceKernel -> rms_norm_kernel route of AllReduceNormKernelLaunch
+ * in "allreduce.d2").  For every row t < tokens and column j < hidden:
+ *
+ *     x[t,j]            = sum_r partials[r][t,j] + bias[j] + residual[t,j]
+ *     residual_out[t,j] = x[t,j]                               (pre-norm sum)
+ *     out[t,j]          = x[t,j] / sqrt(mean_j(x[t,:]^2) + eps) * weight[j]
+ *
+ * The pages name the fields but print no formula; this is the textbook
+ * RMSNorm (eps inside the square root, no mean subtraction, no offset).
+ * x is accumulated in fp32 in the order partials[0..R-1], bias, residual.
+ *
+ *   partials      host array of R device pointers, each [tokens, hidden]
+ *   bias          device [hidden], or NULL for no bias (the GEMM bias,
+ *                 added once after the sum, not once per rank)
+ *   residual      device [tokens, hidden]
+ *   weight        device [hidden]
+ *   eps           float, >= 0 (AllReduceFusionParams::eps is a float)
+ *   out           device [tokens, hidden]: the normalised rows
+ *   residual_out  device [tokens, hidden]: the pre-norm sum x, which the
+ *                 pages call intermediate_buffer; may equal residual
+ *   intermediate  device workspace for AR_TWOSHOT (fp32 per-chunk sums of
+ *                 squares); may be NULL for AR_ONESHOT
+ *   intermediate_bytes  its size; at least ar_workspace_size_rows(...)
+ *   strategy      AR_ONESHOT: one kernel, each row held on chip between the
+ *                 sum and the norm (one pass over HBM).
+ *                 AR_TWOSHOT: phase 1 writes residual_out and the per-chunk
+ *                 sums of squares, phase 2 normalises residual_out.
+ *                 AR_AUTO: chosen by ar_query_strategy; falls back to
+ *                 ONESHOT when the workspace is missing or too small.
+ * Errors: AR_ERR_INVALID_ARG (R out of range, hidden < 1, tokens < 0, NULL
+ *         required pointer, eps < 0 or not finite, out == residual_out),
+ *         AR_ERR_UNSUPPORTED (AR_NCCL, unknown dtype or strategy, a row too
+ *         long for AR_ONESHOT), AR_ERR_WORKSPACE (AR_TWOSHOT without a large
+ *         enough workspace), AR_ERR_CUDA.
+ */
+int ar_residual_rmsnorm(const void* const* partials, int R, const void* bias,
+                        const void* residual, const void* weight, float eps,
+                        int hidden, int tokens, void* out, void* residual_out,
+                        void* intermediate, size_t intermediate_bytes,
+                        int dtype, int strategy, ar_stream_t stream);
+
+/*
+ * ar_params -- one structure holding every argument, after AllReduceParams
+ * (elts_total, peer_comm_buffer_ptrs, local_output_buffer_ptr) and its
+ * AllReduceFusionParams member (bias_buffer, residual_buffer, hidden_size,
+ * weight_buffer, eps, intermediate_buffer) in "type.d2".  local_rank and
+ * deserialize() have no counterpart: there are no peer processes.
+ */
+typedef struct {
+    const void* partials[AR_MAX_RANKS]; /* peer_comm_buffer_ptrs, first R used */
+    int R;
+    int dtype;                          /* ar_dtype */
+    size_t n;                           /* elts_total (tokens * hidden when fused) */
+    void* out;                          /* local_output_buffer_ptr */
+    const void* bias;                   /* bias_buffer, nullable */
+    const void* residual;               /* residual_buffer */
+    const void* weight;                 /* weight_buffer */
+    float eps;                          /* eps */
+    int hidden;                         /* hidden_size */
+    void* residual_out;                 /* intermediate_buffer: the pre-norm sum */
+    void* workspace;                    /* two-shot sums of squares */
+    size_t workspace_bytes;
+} ar_params;
+
+/* Dispatch on the fusion op, after customAllReduce -> AllReduceDispatchMemcpy
+ * ("allreduce.d2"): AR_FUSION_NONE calls ar_sum (bias, residual, weight,
+ * residual_out and workspace ignored); AR_FUSION_RESIDUAL_RMS_NORM calls
+ * ar_residual_rmsnorm with tokens = n / hidden (n must be a multiple of
+ * hidden).  Same errors as those two; AR_ERR_INVALID_ARG for a NULL p. */
+int ar_allreduce(const ar_params* p, int fusion_op, int strategy, ar_stream_t stream);
+
+/*
+ * ar_query_strategy -- what AR_AUTO resolves to (the selectImplementation /
+ * kernelLaunchConfig / heuristic_min_warp_number analogue, "allreduce.d2").
+ * For the fused op n = tokens * hidden.  *chosen receives AR_ONESHOT or
+ * AR_TWOSHOT; *warps_per_token (nullable) receives the warps that cooperate
+ * on one row in the one-shot fused kernel (0 for the reduce-only op, and
+ * for the two-shot fused op, whose blocks each cover a chunk of a row).
+ * The choice assumes a workspace is available.
+ * Errors: AR_ERR_INVALID_ARG, AR_ERR_UNSUPPORTED.
+ */
+int ar_query_strategy(int R, size_t n, int hidden, int dtype, int fusion_op,
+                      int* chosen, int* warps_per_token);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TENSOR_ALLREDUCE_RESIDUAL_AR_H */

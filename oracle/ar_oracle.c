@@ -161,12 +161,14 @@ static void store(void* buf, size_t i, int dtype, double v)
     }
 }
 
-/* out[i] = sum over r = 0..R-1 of partials[r][i], in binary64, rounded once. */
+/* out[i] = partials[0][i] + partials[1][i] + ... + partials[R-1][i], a left
+ * fold in binary64 starting from the first term (so a single partial, -0
+ * included, passes through unchanged), rounded once. */
 void or_sum(const void* const* partials, int R, size_t n, int dtype, void* out)
 {
     for (size_t i = 0; i < n; ++i) {
-        double acc = 0.0;
-        for (int r = 0; r < R; ++r)
+        double acc = load(partials[0], i, dtype);
+        for (int r = 1; r < R; ++r)
             acc += load(partials[r], i, dtype);
         store(out, i, dtype, acc);
     }
@@ -187,8 +189,8 @@ void or_residual_rmsnorm(const void* const* partials, int R, const void* bias,
         size_t row = (size_t)t * (size_t)hidden;
         double sumsq = 0.0;
         for (int j = 0; j < hidden; ++j) {
-            double x = 0.0;
-            for (int r = 0; r < R; ++r)
+            double x = load(partials[0], row + j, dtype);
+            for (int r = 1; r < R; ++r)
                 x += load(partials[r], row + j, dtype);
             if (bias)
                 x += load(bias, (size_t)j, dtype);

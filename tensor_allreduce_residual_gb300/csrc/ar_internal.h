@@ -1,0 +1,77 @@
+// ar_internal.h -- kernel argument blocks and launcher declarations shared by
+// the host dispatch (ar_api.cu) and the per-dtype kernel translation units.
+//
+// The argument blocks are passed BY VALUE as kernel parameters (well under
+// the 4 KB parameter limit), the way AllReduceParams carries
+// peer_comm_buffer_ptrs[MAX_RANKS_PER_NODE] into the kernels ("type.d2",
+// AllReduceParams): the R partial pointers travel with the launch, so the
+// library needs no device-side pointer table and no allocation.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace ar {
+
+constexpr int kMaxRanks = 16;
+
+// Threads per block of the flat kernels (reduce-only, two-shot phases).
+constexpr int kFlatThreads = 256;
+
+// Two-shot fused path: vectors per thread per chunk.  A chunk is
+// kFlatThreads * kChunkVPT packed vectors of one row.
+constexpr int kChunkVPT = 2;
+
+// One-shot fused path: the largest number of packed vectors (or scalar
+// elements on the element-wise path) a thread keeps in registers, and the
+// largest number of threads cooperating on one row.
+constexpr int kMaxVPTVec = 8;
+constexpr int kMaxVPTScalar = 16;
+constexpr int kMaxTPR = 1024;
+
+struct SumArgs {
+    const void* partials[kMaxRanks];
+    void* out;
+    int R;
+    uint32_t tail;      // elements after the last full vector (packed path only)
+    uint64_t nunits;    // full 16-byte vectors (packed path) or elements (element-wise path)
+    uint64_t slice;     // units per slice: nunits (one-shot) or ~nunits/R (two-shot)
+};
+
+struct FusedArgs {
+    const void* partials[kMaxRanks];
+    const void* bias;      // nullable
+    const void* residual;
+    const void* weight;
+    void* out;
+    void* residual_out;
+    float* sumsq;          // two-shot workspace: [tokens, nchunk] fp32
+    int R;
+    int hidden;
+    int tokens;
+    int units_row;         // packed vectors per row (packed path) or hidden (element-wise)
+    int nchunk;            // two-shot chunks per row
+    int chunk_units;       // two-shot units per chunk
+    float eps;
+};
+
+// One-shot fused launch shape: `tpr` threads per row (a power of two),
+// `vpt` units per thread, `rows` rows per block.
+struct OneShotShape {
+    int tpr;
+    int vpt;
+    int rows;
+};
+
+// Launchers, explicitly instantiated for float, __half and __nv_bfloat16 in
+// the per-dtype translation units.  Each returns the cudaError_t of the launch.
+template <typename T>
+cudaError_t launch_sum(const SumArgs& a, bool packed, int nslices, cudaStream_t s);
+
+template <typename T>
+cudaError_t launch_fused_oneshot(const FusedArgs& a, bool packed, OneShotShape shape, cudaStream_t s);
+
+template <typename T>
+cudaError_t launch_fused_twoshot(const FusedArgs& a, bool packed, cudaStream_t s);
+
+}  // namespace ar

@@ -286,3 +286,14 @@ def test_fused_permutation_invariant(dtype):
     a = oracle.residual_rmsnorm(inp.partials, inp.bias, inp.residual, inp.weight, inp.eps, dtype)
     b = oracle.residual_rmsnorm(inp.partials[::-1], inp.bias, inp.residual, inp.weight, inp.eps, dtype)
     assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
+
+
+@pytest.mark.parametrize("dtype", ["fp32", "fp16", "bf16"])
+def test_sum_signed_zero_passthrough(dtype):
+    """tpSize=1 is a passthrough, so a lone -0 stays -0; -0 + -0 is -0 (IEEE)."""
+    neg = torch.full((16,), -0.0, dtype=TD[dtype])
+    one = oracle.sum([neg], dtype)
+    two = oracle.sum([neg, neg.clone()], dtype)
+    assert torch.all(torch.signbit(one)) and torch.all(torch.signbit(two))
+    mixed = oracle.sum([neg, torch.zeros(16, dtype=TD[dtype])], dtype)
+    assert not torch.any(torch.signbit(mixed))        # -0 + +0 = +0 (round to nearest)
