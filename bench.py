@@ -1,0 +1,459 @@
+#!/usr/bin/env python3
+"""Benchmark: the fused R-way sum + bias + residual + RMSNorm on GB300.
+
+One step = one ar_residual_rmsnorm call over the TP prefill workload
+(R=8 bf16 partials, tokens=8192 per GPU, hidden=8192, bias, residual, weight,
+eps=1e-6) through the C ABI, inputs resident in HBM.  `value` is effective
+HBM GB/s over all GPUs (algorithmic bytes = R*n*s + residual + bias + weight
++ both outputs, per call), the unit of the headline metric; `us_per_call`
+gives the other half of it.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Multi-GPU (torchrun, one rank per GPU): each rank owns its own block of
+8192 token rows (weak scaling, no data-path collective); time is the max over
+ranks.  `--impl reference` times the CPU oracle on a bounded sample of the
+same workload instead (rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import datetime as _dt
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "µs/call and effective HBM GB/s (fraction of GB300 peak) for R-way reduce+RMSNorm"
+WORKLOAD = "TP prefill: R=8 bf16 partials, tokens=8192 per GPU, hidden=8192, bias, residual, RESIDUAL_RMS_NORM, eps=1e-6"
+R, TOKENS, HIDDEN, EPS = 8, 8192, 8192, 1e-6
+DATA = ("synthetic, seeded: partials N(0,1/8), residual N(0,4), bias N(0,0.02), weight N(1,0.05) "
+        "(second argument = variance), drawn in fp32 and rounded to bf16")
+FALLBACK_HBM_GBS = 6800.0
+KERNEL_SOURCES = ["ar_kernels.cuh", "ar_launch.cuh", "ar_internal.h", "ar_api.cu"]
+
+
+def parse_args():
+    p = argparse.ArgumentParser(description=__doc__.split("\n")[1])
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=1000)
+    p.add_argument("--warmup", type=int, default=20)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--strategy", default="AUTO", choices=["AUTO", "ONESHOT", "TWOSHOT"])
+    p.add_argument("--e2e-steps", type=int, default=10)
+    p.add_argument("--no-extras", action="store_true", help="skip the secondary workloads")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    return p.parse_args()
+
+
+# ----------------------------------------------------------------------------- helpers
+
+def algorithmic_bytes(R_, T, H, s, has_bias=True):
+    n = T * H
+    return R_ * n * s + n * s + (H * s if has_bias else 0) + H * s + 2 * n * s
+
+
+def kernel_sources_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "tensor_allreduce_residual_gb300", "csrc")
+    for f in KERNEL_SOURCES:
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "of measured"
+    return FALLBACK_HBM_GBS, "of fallback"
+
+
+def profiled_traffic(kernel_tag: str):
+    """dram bytes per launch from a committed ncu summary, if it was taken on the current kernel sources."""
+    pdir = os.path.join(ROOT, "profiles")
+    if not os.path.isdir(pdir):
+        return None
+    want = kernel_sources_hash()
+    for name in sorted(os.listdir(pdir)):
+        if not name.endswith(".md"):
+            continue
+        text = open(os.path.join(pdir, name)).read()
+        m_tag = re.search(r"^roofline_kernel:\s*(\S+)", text, re.M)
+        m_hash = re.search(r"^kernel_sources_sha256:\s*(\S+)", text, re.M)
+        m_tr = re.search(r"^traffic_bytes_per_launch:\s*([0-9.eE+]+)", text, re.M)
+        if m_tag and m_hash and m_tr and m_tag.group(1) == kernel_tag and m_hash.group(1) == want:
+            return float(m_tr.group(1))
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples while the GPU works."""
+    FIELDS = ("timestamp,uuid,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, uuids):
+        self.uuids = {u.lower().replace("gpu-", "") for u in uuids}
+        self.proc = None
+        self.file = None
+
+    def start(self):
+        self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "50"]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=self.file, stderr=subprocess.DEVNULL)
+        except (OSError, ValueError):
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        self.file.flush()
+        self.file.seek(0)
+        rows = []
+        for line in self.file:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) != 10:
+                continue
+            try:
+                ts = _dt.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                rows.append({"t": ts, "uuid": parts[1].lower().replace("gpu-", ""),
+                             "sm": float(parts[2]), "sm_max": float(parts[3]),
+                             "power": float(parts[4]) if parts[4] not in ("[N/A]", "") else None,
+                             "hw": parts[6], "hw_thermal": parts[7], "sw_thermal": parts[8], "sw_power": parts[9]})
+            except ValueError:
+                continue
+        self.file.close()
+        os.unlink(self.file.name)
+        mine = [r for r in rows if r["uuid"] in self.uuids]
+        return mine if mine else rows   # uuid not matched: every visible GPU
+
+    @staticmethod
+    def summarize(rows, t0, t1):
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        window = [r for r in rows if t0 - 0.05 <= r["t"] <= t1 + 0.05]
+        if not window:  # region shorter than the sampling period: the nearest sample
+            window = [min(rows, key=lambda r: abs(r["t"] - (t0 + t1) / 2))]
+        reasons = set()
+        for r in window:
+            for key, name in (("hw", "hw_slowdown"), ("hw_thermal", "hw_thermal_slowdown"),
+                              ("sw_thermal", "sw_thermal_slowdown"), ("sw_power", "sw_power_cap")):
+                if r[key].lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(r["sm"] for r in window),
+                "sm_max_mhz": max(r["sm_max"] for r in window),
+                "reasons": sorted(reasons), "samples": len(window)}
+
+
+# ----------------------------------------------------------------------------- our arm
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+    import torch.distributed as dist
+
+    import tensor_allreduce_residual_gb300 as ar
+    import workloads
+    from tensor_allreduce_residual_gb300.dist import max_over_ranks
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    ar.lib()  # raises if the CUDA library is missing: there is no other path
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    # Inputs: this rank's block of rows, drawn on the GPU (seeded per rank).
+    inp = workloads.tp_prefill(TOKENS, HIDDEN, seed=rank, device="cuda")
+    parts, resid, weight, bias = inp.partials, inp.residual, inp.weight, inp.bias
+    out = torch.empty_like(resid)
+    res_out = torch.empty_like(resid)
+    ws = torch.empty(ar.ar_workspace_size_rows(R, HIDDEN, TOKENS, ar.AR_BF16), dtype=torch.uint8, device=dev)
+    bytes_call = algorithmic_bytes(R, TOKENS, HIDDEN, 2)
+    stream = torch.cuda.current_stream()
+    chosen, warps = ar.ar_query_strategy(R, TOKENS * HIDDEN, HIDDEN, ar.AR_BF16)
+    resolved = ar.STRATEGY_NAMES[chosen] if args.strategy == "AUTO" else args.strategy
+    launches_per_step = 1 if resolved == "ONESHOT" else 2
+
+    def step(strategy=args.strategy):
+        ar.ar_residual_rmsnorm(parts, resid, weight, EPS, bias=bias, out=out, residual_out=res_out,
+                               intermediate=ws, strategy=strategy, stream=stream)
+
+    uuids = [str(torch.cuda.get_device_properties(dev).uuid)]
+    if world > 1:
+        gathered = [None] * world
+        dist.all_gather_object(gathered, uuids[0])
+        uuids = gathered
+    sampler = ClockSampler(uuids) if rank == 0 else None
+    if sampler:
+        sampler.start()
+
+    for _ in range(args.warmup):
+        step()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    t_begin, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    wall0 = time.time()
+    t_begin.record(stream)
+    for s0, s1 in ev:
+        s0.record(stream)
+        step()
+        s1.record(stream)
+    t_end.record(stream)
+    barrier()
+    wall1 = time.time()
+    region_ms = t_begin.elapsed_time(t_end)
+    per_step = [a.elapsed_time(b) for a, b in ev]
+    clocks = ClockSampler.summarize(sampler.stop(), wall0, wall1) if sampler else None
+    region_ms_max = max_over_ranks(region_ms, dev)
+
+    value = bytes_call * world * args.steps / (region_ms_max * 1e-3) / 1e9
+    ms_step = region_ms_max / args.steps
+    peak, peak_src = measured_peaks()
+    mean_launch_ms = statistics.fmean(per_step)
+    achieved = bytes_call / (mean_launch_ms * 1e-3) / 1e9
+    kernel_tag = "k_fused_oneshot" if resolved == "ONESHOT" else "k_twoshot_phase1+phase2"
+    traffic = profiled_traffic(kernel_tag)
+    roofline = {"bound": "hbm", "kernel": kernel_tag, "achieved": round(achieved, 1), "peak": peak,
+                "unit": "GB/s", "frac": round(achieved / peak, 4), "peak_source": peak_src,
+                "traffic": traffic, "algorithmic_bytes_per_launch": bytes_call,
+                "launch_ms_mean": round(mean_launch_ms, 5), "launch_ms_median": round(statistics.median(per_step), 5)}
+
+    # End to end through the same C-ABI call: host (pinned) inputs copied in and
+    # both outputs copied back inside the timed region, every step.
+    host_in = [t.cpu().pin_memory() for t in parts + [resid, weight, bias]]
+    dev_in = parts + [resid, weight, bias]
+    host_out = [torch.empty(out.shape, dtype=out.dtype).pin_memory() for _ in range(2)]
+    h2d = sum(t.numel() * t.element_size() for t in host_in)
+    d2h = sum(t.numel() * t.element_size() for t in host_out)
+
+    def e2e_step():
+        for d, h in zip(dev_in, host_in):
+            d.copy_(h, non_blocking=True)
+        step()
+        host_out[0].copy_(out, non_blocking=True)
+        host_out[1].copy_(res_out, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    barrier()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), dev)
+    e2e = {"value": round(bytes_call * world * args.e2e_steps / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": args.e2e_steps,
+           "us_per_call": round(e2e_ms * 1e3 / args.e2e_steps, 1),
+           "note": "pinned host inputs copied in and both outputs copied out inside the timed region"}
+    del host_in, host_out
+
+    extras = None
+    if not args.no_extras and rank == 0:
+        extras = run_extras(ar, torch, workloads, parts, resid, weight, bias, out, res_out, ws, bytes_call, stream)
+
+    if rank != 0:
+        return None
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_step, 5), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": DATA,
+        "config": {"workload": WORKLOAD, "R": R, "tokens_per_gpu": TOKENS, "global_tokens": TOKENS * world,
+                   "hidden": HIDDEN, "io_dtype": "bf16", "eps": EPS, "strategy": args.strategy,
+                   "resolved_strategy": resolved, "warps_per_token": warps,
+                   "bytes_per_call": bytes_call, "parallelism": f"rows sharded over {world} GPU(s), no collective",
+                   "l2": "inputs larger than L2 (1.48 GB per call vs 129 MB L2): no flush between steps"},
+        "us_per_call": round(ms_step * 1e3, 2), "frac_of_peak": round(value / world / peak, 4),
+        "clocks": clocks, "e2e": e2e, "gpu_launches": launches_per_step * args.steps, "roofline": roofline,
+    }
+    if extras is not None:
+        line["extras"] = extras
+    return line
+
+
+def _time_calls(torch, fn, stream, n, warm=3):
+    for _ in range(warm):
+        fn()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    a.record(stream)
+    for _ in range(n):
+        fn()
+    b.record(stream)
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) / n
+
+
+def _time_cold(torch, fn, stream, flush, n):
+    """Median per-call time with L2 flushed (a 256 MB write) before every call."""
+    ts = []
+    for _ in range(n):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        fn()
+        b.record(stream)
+        torch.cuda.synchronize()
+        ts.append(a.elapsed_time(b))
+    return statistics.median(ts)
+
+
+def run_extras(ar, torch, workloads, parts, resid, weight, bias, out, res_out, ws, bytes_call, stream):
+    """Secondary numbers: each fixed strategy on the prefill inputs, decode latency, reduce-only bandwidth."""
+    ex = {}
+    for s in ("ONESHOT", "TWOSHOT"):
+        ms = _time_calls(torch, lambda s=s: ar.ar_residual_rmsnorm(
+            parts, resid, weight, EPS, bias=bias, out=out, residual_out=res_out, intermediate=ws,
+            strategy=s, stream=stream), stream, 100)
+        ex[f"prefill_{s}"] = {"us_per_call": round(ms * 1e3, 2), "GBps": round(bytes_call / ms / 1e6, 1)}
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    dec = {}
+    for T in (1, 8, 32):
+        f = workloads.tp_decode(T, device="cuda")
+        o, r = torch.empty_like(f.residual), torch.empty_like(f.residual)
+        fn = lambda f=f, o=o, r=r: ar.ar_residual_rmsnorm(f.partials, f.residual, f.weight, f.eps, bias=f.bias,  # noqa: E731
+                                                          out=o, residual_out=r, strategy="ONESHOT", stream=stream)
+        dec[f"T{T}"] = {"us_warm": round(_time_calls(torch, fn, stream, 200) * 1e3, 2),
+                        "us_cold": round(_time_cold(torch, fn, stream, flush, 30) * 1e3, 2)}
+    ex["tp_decode_R2_fp16_H4096"] = dec
+    r8 = {}
+    for T in workloads.DECODE_R8_TOKENS:
+        f = workloads.decode_r8(T, device="cuda")
+        o, r = torch.empty_like(f.residual), torch.empty_like(f.residual)
+        w8 = torch.empty(ar.ar_workspace_size_rows(8, 8192, T, ar.AR_BF16), dtype=torch.uint8, device="cuda")
+        fn = lambda f=f, o=o, r=r, w8=w8: ar.ar_residual_rmsnorm(f.partials, f.residual, f.weight, f.eps,  # noqa: E731
+                                                                 out=o, residual_out=r, intermediate=w8,
+                                                                 strategy="AUTO", stream=stream)
+        b = algorithmic_bytes(8, T, 8192, 2, has_bias=False)
+        cold = _time_cold(torch, fn, stream, flush, 30)
+        r8[f"T{T}"] = {"us_warm": round(_time_calls(torch, fn, stream, 100) * 1e3, 2), "us_cold": round(cold * 1e3, 2),
+                       "GBps_cold": round(b / cold / 1e6, 1),
+                       "auto": ar.STRATEGY_NAMES[ar.ar_query_strategy(8, T * 8192, 8192, ar.AR_BF16)[0]]}
+    ex["decode_R8_bf16_H8192"] = r8
+    del flush
+    red = {}
+    n = 1 << 27
+    s_in = workloads.reduce_only(n, device="cuda")
+    o = torch.empty_like(s_in.partials[0])
+    b = workloads.sum_algorithmic_bytes(4, n, "fp16")
+    for s in ("ONESHOT", "TWOSHOT"):
+        ms = _time_calls(torch, lambda s=s: ar.ar_sum(s_in.partials, out=o, strategy=s, stream=stream), stream, 20)
+        red[s] = {"us_per_call": round(ms * 1e3, 1), "GBps": round(b / ms / 1e6, 1)}
+    ex["reduce_only_R4_fp16_n2^27"] = red
+    del s_in, o
+    torch.cuda.empty_cache()
+    return ex
+
+
+# ----------------------------------------------------------------------------- the oracle
+
+def oracle_sample(rows: int):
+    import workloads
+    return workloads.tp_prefill(tokens=rows, hidden=HIDDEN, seed=0)
+
+
+def cpu_baseline(target_s: float = 10.0, rows: int = 512):
+    """The CPU oracle, as it stands, on a bounded sample of the workload's rows (1 core)."""
+    import oracle
+    oracle.build()
+    inp = oracle_sample(rows)
+    b = algorithmic_bytes(R, rows, HIDDEN, 2)
+    calls, t0 = 0, time.perf_counter()
+    while True:
+        oracle.residual_rmsnorm(inp.partials, inp.bias, inp.residual, inp.weight, inp.eps, "bf16")
+        calls += 1
+        el = time.perf_counter() - t0
+        if el >= target_s:
+            break
+    return {"value": round(b * calls / el / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"{calls} calls x {rows} rows of the workload (R=8 bf16, hidden=8192), {el:.1f} s, "
+                      f"single-threaded binary64 C, host {os.uname().machine}"}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return None
+    import oracle
+    oracle.build()
+    rows = 64 if args.steps <= 200 else max(1, int(64 * 200 / args.steps))
+    inp = oracle_sample(rows)
+    b = algorithmic_bytes(R, rows, HIDDEN, 2)
+    call = lambda: oracle.residual_rmsnorm(inp.partials, inp.bias, inp.residual, inp.weight, inp.eps, "bf16")  # noqa: E731
+    for _ in range(args.warmup):
+        call()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        call()
+    el = time.perf_counter() - t0
+    value = b * args.steps / el / 1e9
+    ms = el * 1e3 / args.steps
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": DATA,
+        "config": {"workload": WORKLOAD, "R": R, "tokens_per_gpu": TOKENS, "hidden": HIDDEN, "io_dtype": "bf16",
+                   "eps": EPS, "sample_rows_per_step": rows},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": f"{rows} rows of the workload per step, single-threaded binary64 C oracle"},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+# ----------------------------------------------------------------------------- main
+
+def main():
+    args = parse_args()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.warmup < 3:
+        print("bench.py: --warmup must be >= 3", file=sys.stderr)
+        return 2
+    if world > 1 and args.impl == "reference":
+        line = run_reference(args, rank, world)
+        if line:
+            print(json.dumps(line), flush=True)
+        return 0
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    try:
+        if args.impl == "reference":
+            line = run_reference(args, rank, world)
+        else:
+            line = run_ours(args, rank, world, local_rank)
+            if line is not None and world == 1 and not args.no_cpu_baseline:
+                line["cpu_baseline"] = cpu_baseline()
+        if line is not None:
+            print(json.dumps(line), flush=True)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

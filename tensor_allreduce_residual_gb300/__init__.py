@@ -1,0 +1,245 @@
+"""GB300-native R-way all-reduce (sum) and fused sum + residual + RMSNorm.
+
+Thin Python binding of the C-ABI library ``libar.so`` (declared in
+``include/ar.h``).  Every function here only marshals torch tensors into
+pointers and sizes and calls the library function of the same name; all
+arithmetic runs in the library's CUDA kernels.  There is no fallback: if the
+library has not been built, or no CUDA device is present, calls raise.
+
+The R partials are R CUDA tensors on the same device: the tensor-parallel
+ranks' partial outputs of a row-parallel linear layer, kept in one GPU's HBM.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional, Sequence
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libar.so")
+
+# ar_dtype
+AR_FP32, AR_FP16, AR_BF16 = 0, 1, 2
+# ar_strategy (AllReduceStrategyType values)
+AR_NCCL, AR_ONESHOT, AR_TWOSHOT, AR_AUTO = 0, 1, 2, 3
+# ar_fusion_op (AllReduceFusionOp values)
+AR_FUSION_NONE, AR_FUSION_RESIDUAL_RMS_NORM = 0, 1
+# status codes
+AR_OK, AR_ERR_INVALID_ARG, AR_ERR_UNSUPPORTED, AR_ERR_WORKSPACE, AR_ERR_CUDA = 0, -1, -2, -3, -4
+AR_MAX_RANKS = 16
+
+STRATEGIES = {"NCCL": AR_NCCL, "ONESHOT": AR_ONESHOT, "TWOSHOT": AR_TWOSHOT, "AUTO": AR_AUTO}
+STRATEGY_NAMES = {v: k for k, v in STRATEGIES.items()}
+_TORCH_TO_AR = {torch.float32: AR_FP32, torch.float16: AR_FP16, torch.bfloat16: AR_BF16}
+
+
+class ARError(RuntimeError):
+    """A non-zero status returned by the library."""
+
+    def __init__(self, func: str, status: int):
+        self.status = status
+        super().__init__(f"{func} failed: {status} ({ar_strerror(status)})")
+
+
+class ArParams(ctypes.Structure):
+    """Mirror of the C struct ar_params."""
+    _fields_ = [
+        ("partials", ctypes.c_void_p * AR_MAX_RANKS),
+        ("R", ctypes.c_int),
+        ("dtype", ctypes.c_int),
+        ("n", ctypes.c_size_t),
+        ("out", ctypes.c_void_p),
+        ("bias", ctypes.c_void_p),
+        ("residual", ctypes.c_void_p),
+        ("weight", ctypes.c_void_p),
+        ("eps", ctypes.c_float),
+        ("hidden", ctypes.c_int),
+        ("residual_out", ctypes.c_void_p),
+        ("workspace", ctypes.c_void_p),
+        ("workspace_bytes", ctypes.c_size_t),
+    ]
+
+
+_lib: Optional[ctypes.CDLL] = None
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded libar.so with its C signatures declared.  Raises if it is not built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError(f"{LIB_PATH} is missing: build it first (tensor_allreduce_residual_gb300._build.build())")
+    L = ctypes.CDLL(LIB_PATH)
+    vp, sz, i = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int
+    pvp = ctypes.POINTER(ctypes.c_void_p)
+    L.ar_version.argtypes, L.ar_version.restype = [], i
+    L.ar_strerror.argtypes, L.ar_strerror.restype = [i], ctypes.c_char_p
+    L.ar_workspace_size.argtypes, L.ar_workspace_size.restype = [i, sz, i], sz
+    L.ar_workspace_size_rows.argtypes, L.ar_workspace_size_rows.restype = [i, i, i, i], sz
+    L.ar_sum.argtypes, L.ar_sum.restype = [pvp, i, vp, sz, i, i, vp], i
+    L.ar_residual_rmsnorm.argtypes = [pvp, i, vp, vp, vp, ctypes.c_float, i, i, vp, vp, vp, sz, i, i, vp]
+    L.ar_residual_rmsnorm.restype = i
+    L.ar_allreduce.argtypes, L.ar_allreduce.restype = [ctypes.POINTER(ArParams), i, i, vp], i
+    L.ar_query_strategy.argtypes = [i, sz, i, i, i, ctypes.POINTER(i), ctypes.POINTER(i)]
+    L.ar_query_strategy.restype = i
+    _lib = L
+    return L
+
+
+# ------------------------------------------------------------------ helpers
+
+def dtype_code(dtype: torch.dtype) -> int:
+    try:
+        return _TORCH_TO_AR[dtype]
+    except KeyError:
+        raise ValueError(f"unsupported dtype {dtype}; expected float32, float16 or bfloat16") from None
+
+
+def _strategy(s) -> int:
+    return STRATEGIES[s.upper()] if isinstance(s, str) else int(s)
+
+
+def _ptr_array(ptrs):
+    arr = (ctypes.c_void_p * max(1, len(ptrs)))()
+    for k, p in enumerate(ptrs):
+        arr[k] = p
+    return arr
+
+
+def _dev_ptr(t: Optional[torch.Tensor], what: str) -> Optional[int]:
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError(f"{what} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{what} must be contiguous")
+    return t.data_ptr()
+
+
+def _stream_handle(stream) -> Optional[int]:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _check(func: str, status: int):
+    if status != AR_OK:
+        raise ARError(func, status)
+
+
+# ------------------------------------------------------------------ the ABI
+
+def ar_version() -> int:
+    return lib().ar_version()
+
+
+def ar_strerror(code: int) -> str:
+    return lib().ar_strerror(code).decode()
+
+
+def ar_workspace_size(R: int, n: int, dtype) -> int:
+    code = dtype if isinstance(dtype, int) else dtype_code(dtype)
+    return int(lib().ar_workspace_size(R, n, code))
+
+
+def ar_workspace_size_rows(R: int, hidden: int, tokens: int, dtype) -> int:
+    code = dtype if isinstance(dtype, int) else dtype_code(dtype)
+    return int(lib().ar_workspace_size_rows(R, hidden, tokens, code))
+
+
+def ar_query_strategy(R: int, n: int, hidden: int, dtype, fusion_op: int = AR_FUSION_RESIDUAL_RMS_NORM):
+    """(strategy code, warps per token) that AR_AUTO picks for this shape."""
+    code = dtype if isinstance(dtype, int) else dtype_code(dtype)
+    chosen, warps = ctypes.c_int(0), ctypes.c_int(0)
+    _check("ar_query_strategy",
+           lib().ar_query_strategy(R, n, hidden, code, fusion_op, ctypes.byref(chosen), ctypes.byref(warps)))
+    return chosen.value, warps.value
+
+
+def ar_sum(partials: Sequence[torch.Tensor], out: Optional[torch.Tensor] = None,
+           strategy="AUTO", stream=None) -> torch.Tensor:
+    """out = sum of the R partial tensors (same shape, dtype and device)."""
+    if len(partials) == 0:
+        raise ValueError("ar_sum needs at least one partial")
+    p0 = partials[0]
+    for k, p in enumerate(partials):
+        if p.shape != p0.shape or p.dtype != p0.dtype or p.device != p0.device:
+            raise ValueError(f"partials[{k}] does not match partials[0] in shape, dtype or device")
+    if out is None:
+        out = torch.empty_like(p0)
+    elif out.numel() != p0.numel() or out.dtype != p0.dtype:
+        raise ValueError("out must match the partials in size and dtype")
+    ptrs = _ptr_array([_dev_ptr(p, f"partials[{k}]") for k, p in enumerate(partials)])
+    status = lib().ar_sum(ptrs, len(partials), _dev_ptr(out, "out"), p0.numel(), dtype_code(p0.dtype),
+                          _strategy(strategy), _stream_handle(stream))
+    _check("ar_sum", status)
+    return out
+
+
+def ar_residual_rmsnorm(partials: Sequence[torch.Tensor], residual: torch.Tensor, weight: torch.Tensor,
+                        eps: float, bias: Optional[torch.Tensor] = None,
+                        out: Optional[torch.Tensor] = None, residual_out: Optional[torch.Tensor] = None,
+                        intermediate: Optional[torch.Tensor] = None, strategy="AUTO", stream=None):
+    """(out, residual_out) of the fused sum + bias + residual + RMSNorm over [tokens, hidden] rows.
+
+    ``intermediate`` is the two-shot workspace (any CUDA tensor of at least
+    ar_workspace_size_rows(...) bytes); when it is None and the strategy may
+    take the two-shot path, one is allocated with torch.
+    """
+    if residual.dim() != 2:
+        raise ValueError("residual must be [tokens, hidden]")
+    tokens, hidden = residual.shape
+    for k, p in enumerate(partials):
+        if p.numel() != residual.numel() or p.dtype != residual.dtype:
+            raise ValueError(f"partials[{k}] must match residual in size and dtype")
+    if out is None:
+        out = torch.empty_like(residual)
+    if residual_out is None:
+        residual_out = torch.empty_like(residual)
+    code = dtype_code(residual.dtype)
+    st = _strategy(strategy)
+    if intermediate is None and st in (AR_TWOSHOT, AR_AUTO):
+        need = ar_workspace_size_rows(len(partials), hidden, tokens, code)
+        if need:
+            intermediate = torch.empty(need, dtype=torch.uint8, device=residual.device)
+    ws_ptr = _dev_ptr(intermediate, "intermediate")
+    ws_bytes = 0 if intermediate is None else intermediate.numel() * intermediate.element_size()
+    ptrs = _ptr_array([_dev_ptr(p, f"partials[{k}]") for k, p in enumerate(partials)])
+    status = lib().ar_residual_rmsnorm(
+        ptrs, len(partials), _dev_ptr(bias, "bias"), _dev_ptr(residual, "residual"),
+        _dev_ptr(weight, "weight"), ctypes.c_float(eps), hidden, tokens, _dev_ptr(out, "out"),
+        _dev_ptr(residual_out, "residual_out"), ws_ptr, ws_bytes, code, st, _stream_handle(stream))
+    _check("ar_residual_rmsnorm", status)
+    return out, residual_out
+
+
+def ar_allreduce(params: ArParams, fusion_op: int, strategy="AUTO", stream=None) -> None:
+    """Calls ar_allreduce with a filled ArParams structure (raw device pointers)."""
+    _check("ar_allreduce", lib().ar_allreduce(ctypes.byref(params), fusion_op, _strategy(strategy),
+                                              _stream_handle(stream)))
+
+
+def make_params(partials, out, *, bias=None, residual=None, weight=None, eps=0.0, hidden=0,
+                residual_out=None, workspace=None) -> ArParams:
+    """Fills an ArParams from tensors (marshalling only)."""
+    p = ArParams()
+    for k, t in enumerate(partials):
+        p.partials[k] = _dev_ptr(t, f"partials[{k}]")
+    p.R = len(partials)
+    p.dtype = dtype_code(partials[0].dtype)
+    p.n = partials[0].numel()
+    p.out = _dev_ptr(out, "out")
+    p.bias = _dev_ptr(bias, "bias")
+    p.residual = _dev_ptr(residual, "residual")
+    p.weight = _dev_ptr(weight, "weight")
+    p.eps = eps
+    p.hidden = hidden
+    p.residual_out = _dev_ptr(residual_out, "residual_out")
+    p.workspace = _dev_ptr(workspace, "workspace")
+    p.workspace_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    return p

@@ -1,0 +1,344 @@
+// ar_api.cu -- the C ABI declared in include/ar.h: argument checks (the
+// configurationSupported analogue), the AUTO choice and launch shape
+// (selectImplementation / kernelLaunchConfig / heuristic_min_warp_number),
+// and dispatch on element type (AllReduceDispatchType) -- all after the
+// call graph of "allreduce.d2".  Host code only; it allocates nothing.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include <cmath>
+#include <cstdint>
+
+#include "ar.h"
+#include "ar_auto_table.h"
+#include "ar_internal.h"
+
+namespace {
+
+using ar::FusedArgs;
+using ar::OneShotShape;
+using ar::SumArgs;
+
+constexpr int kVersion = 10000;  // 1.0.0
+
+int esize_of(int dtype)
+{
+    switch (dtype) {
+    case AR_FP32: return 4;
+    case AR_FP16: return 2;
+    case AR_BF16: return 2;
+    default: return 0;
+    }
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int status_of(cudaError_t e) { return e == cudaSuccess ? AR_OK : AR_ERR_CUDA; }
+
+// Calls f(T{}) with T the element type of `dtype`.
+template <typename F>
+cudaError_t by_dtype(int dtype, F&& f)
+{
+    switch (dtype) {
+    case AR_FP32: return f(float{});
+    case AR_FP16: return f(__half{});
+    default: return f(__nv_bfloat16{});
+    }
+}
+
+int strategy_status(int strategy)
+{
+    if (strategy == AR_ONESHOT || strategy == AR_TWOSHOT || strategy == AR_AUTO)
+        return AR_OK;
+    return AR_ERR_UNSUPPORTED;  // AR_NCCL (no NCCL, one GPU) or unknown
+}
+
+int next_pow2(int v)
+{
+    int p = 1;
+    while (p < v)
+        p <<= 1;
+    return p;
+}
+
+// ---------------------------------------------------------------- one-shot shape
+
+// Threads per row = units_row / vpt rounded up to a power of two, at most
+// kMaxTPR; blocks hold at least 128 threads.  Returns false when the row does
+// not fit in registers (then only the two-shot path can take it).
+bool oneshot_shape(int units_row, int vpt, bool packed, OneShotShape* sh)
+{
+    const int max_vpt = packed ? ar::kMaxVPTVec : ar::kMaxVPTScalar;
+    if (vpt < 1 || vpt > max_vpt)
+        return false;
+    const int tpr = next_pow2((units_row + vpt - 1) / vpt);
+    if (tpr > ar::kMaxTPR || tpr > ar::oneshot_max_threads(vpt))
+        return false;
+    sh->tpr = tpr;
+    sh->vpt = vpt;
+    sh->rows = tpr >= 128 ? 1 : 128 / tpr;
+    return true;
+}
+
+// Rule used when the measured table has no entry: aim for 512 threads per
+// row when there are few rows (more memory parallelism per row) and 256
+// otherwise, with the smallest units-per-thread that reaches it.
+int rule_vpt(int units_row, int tokens, bool packed)
+{
+    const int max_vpt = packed ? ar::kMaxVPTVec : ar::kMaxVPTScalar;
+    const int target = tokens <= 32 ? 512 : 256;
+    int vpt = 1;
+    while (vpt < max_vpt && (units_row + vpt - 1) / vpt > target)
+        vpt <<= 1;
+    while (vpt < max_vpt && next_pow2((units_row + vpt - 1) / vpt) > ar::oneshot_max_threads(vpt))
+        vpt <<= 1;
+    return vpt;
+}
+
+const ar::AutoEntry* table_lookup(int esize, int R, int units_row, int tokens)
+{
+    for (const ar::AutoEntry& e : ar::kAutoTable) {
+        if (e.esize == 0)
+            break;
+        if (e.esize == esize && e.R == R && e.units_row == units_row && tokens <= e.tokens_max)
+            return &e;
+    }
+    return nullptr;
+}
+
+struct FusedPlan {
+    int strategy;      // AR_ONESHOT or AR_TWOSHOT
+    bool oneshot_ok;   // the row fits the one-shot kernel
+    OneShotShape shape;
+};
+
+// Resolves AUTO and the one-shot shape for a fused call.
+FusedPlan plan_fused(int esize, int R, int hidden, int tokens, bool packed, int strategy)
+{
+    const int lanes = 16 / esize;
+    const int units_row = packed ? hidden / lanes : hidden;
+    FusedPlan p{};
+    int vpt = rule_vpt(units_row, tokens, packed);
+    int auto_strategy = AR_ONESHOT;
+    if (packed) {
+        if (const ar::AutoEntry* e = table_lookup(esize, R, units_row, tokens)) {
+            auto_strategy = e->strategy;
+            if (e->vpt > 0)
+                vpt = e->vpt;
+        }
+    }
+    p.oneshot_ok = oneshot_shape(units_row, vpt, packed, &p.shape);
+    if (!p.oneshot_ok)
+        auto_strategy = AR_TWOSHOT;
+    p.strategy = strategy == AR_AUTO ? auto_strategy : strategy;
+    return p;
+}
+
+// Two-shot chunking: chunks of kFlatThreads * kChunkVPT units per row.
+int twoshot_nchunk(int units_row)
+{
+    const int chunk = ar::kFlatThreads * ar::kChunkVPT;
+    return (units_row + chunk - 1) / chunk;
+}
+
+size_t round256(size_t b) { return (b + 255) / 256 * 256; }
+
+}  // namespace
+
+extern "C" {
+
+int ar_version(void) { return kVersion; }
+
+const char* ar_strerror(int code)
+{
+    switch (code) {
+    case AR_OK: return "success";
+    case AR_ERR_INVALID_ARG: return "invalid argument";
+    case AR_ERR_UNSUPPORTED: return "unsupported configuration";
+    case AR_ERR_WORKSPACE: return "workspace missing or too small";
+    case AR_ERR_CUDA: return "CUDA launch error";
+    default: return "unknown status code";
+    }
+}
+
+size_t ar_workspace_size(int R, size_t n, int dtype)
+{
+    if (R < 1 || R > AR_MAX_RANKS || n == 0 || esize_of(dtype) == 0)
+        return 0;
+    // At most one (row, chunk) entry per element: reached by hidden == 1.
+    return round256(n * sizeof(float));
+}
+
+size_t ar_workspace_size_rows(int R, int hidden, int tokens, int dtype)
+{
+    if (R < 1 || R > AR_MAX_RANKS || hidden < 1 || tokens < 0 || esize_of(dtype) == 0)
+        return 0;
+    // The element-wise path (hidden not a multiple of the lane count, or a
+    // misaligned pointer) has the most chunks; size for it.
+    return round256(static_cast<size_t>(tokens) * twoshot_nchunk(hidden) * sizeof(float));
+}
+
+int ar_sum(const void* const* partials, int R, void* out, size_t n, int dtype, int strategy,
+           ar_stream_t stream)
+{
+    if (R < 1 || R > AR_MAX_RANKS)
+        return AR_ERR_INVALID_ARG;
+    const int esize = esize_of(dtype);
+    if (esize == 0)
+        return AR_ERR_UNSUPPORTED;
+    if (int st = strategy_status(strategy))
+        return st;
+    if (n == 0)
+        return AR_OK;
+    if (partials == nullptr || out == nullptr)
+        return AR_ERR_INVALID_ARG;
+    bool packed = aligned16(out);
+    for (int r = 0; r < R; ++r) {
+        if (partials[r] == nullptr)
+            return AR_ERR_INVALID_ARG;
+        packed = packed && aligned16(partials[r]);
+    }
+    if (R == 1 && partials[0] == out)
+        return AR_OK;  // tpSize == 1 passthrough, in place: nothing to do
+
+    SumArgs a{};
+    for (int r = 0; r < R; ++r)
+        a.partials[r] = partials[r];
+    a.out = out;
+    a.R = R;
+    const int lanes = 16 / esize;
+    a.nunits = packed ? n / lanes : n;
+    a.tail = packed ? static_cast<uint32_t>(n % lanes) : 0u;
+
+    // Both strategies give bit-identical values; AUTO takes the one-shot
+    // partition (the two-shot slices only change which block reads what).
+    int nslices = 1;
+    if (strategy == AR_TWOSHOT && R > 1) {
+        a.slice = (a.nunits + R - 1) / R;
+        nslices = a.slice == 0 ? 1 : R;
+    }
+    if (nslices == 1)
+        a.slice = a.nunits;
+
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    return status_of(by_dtype(dtype, [&](auto tag) {
+        using T = decltype(tag);
+        return ar::launch_sum<T>(a, packed, nslices, s);
+    }));
+}
+
+int ar_residual_rmsnorm(const void* const* partials, int R, const void* bias, const void* residual,
+                        const void* weight, float eps, int hidden, int tokens, void* out,
+                        void* residual_out, void* intermediate, size_t intermediate_bytes, int dtype,
+                        int strategy, ar_stream_t stream)
+{
+    if (R < 1 || R > AR_MAX_RANKS || hidden < 1 || tokens < 0)
+        return AR_ERR_INVALID_ARG;
+    const int esize = esize_of(dtype);
+    if (esize == 0)
+        return AR_ERR_UNSUPPORTED;
+    if (int st = strategy_status(strategy))
+        return st;
+    if (!std::isfinite(eps) || eps < 0.0f)
+        return AR_ERR_INVALID_ARG;
+    if (tokens == 0)
+        return AR_OK;
+    if (partials == nullptr || residual == nullptr || weight == nullptr || out == nullptr ||
+        residual_out == nullptr || out == residual_out)
+        return AR_ERR_INVALID_ARG;
+    const int lanes = 16 / esize;
+    bool packed = hidden % lanes == 0 && aligned16(residual) && aligned16(weight) &&
+                  aligned16(out) && aligned16(residual_out) && (bias == nullptr || aligned16(bias));
+    for (int r = 0; r < R; ++r) {
+        if (partials[r] == nullptr)
+            return AR_ERR_INVALID_ARG;
+        packed = packed && aligned16(partials[r]);
+    }
+
+    FusedPlan plan = plan_fused(esize, R, hidden, tokens, packed, strategy);
+    const int units_row = packed ? hidden / lanes : hidden;
+    const int nchunk = twoshot_nchunk(units_row);
+    const size_t ws_need = static_cast<size_t>(tokens) * nchunk * sizeof(float);
+    const bool ws_ok = intermediate != nullptr && intermediate_bytes >= ws_need &&
+                       (reinterpret_cast<uintptr_t>(intermediate) & 3u) == 0;
+    if (plan.strategy == AR_TWOSHOT && !ws_ok) {
+        if (strategy == AR_AUTO && plan.oneshot_ok)
+            plan.strategy = AR_ONESHOT;  // AUTO without workspace: stay one-shot
+        else
+            return AR_ERR_WORKSPACE;
+    }
+    if (plan.strategy == AR_ONESHOT && !plan.oneshot_ok)
+        return AR_ERR_UNSUPPORTED;
+
+    FusedArgs a{};
+    for (int r = 0; r < R; ++r)
+        a.partials[r] = partials[r];
+    a.bias = bias;
+    a.residual = residual;
+    a.weight = weight;
+    a.out = out;
+    a.residual_out = residual_out;
+    a.sumsq = static_cast<float*>(intermediate);
+    a.R = R;
+    a.hidden = hidden;
+    a.tokens = tokens;
+    a.units_row = units_row;
+    a.nchunk = nchunk;
+    a.chunk_units = ar::kFlatThreads * ar::kChunkVPT;
+    a.eps = eps;
+
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    return status_of(by_dtype(dtype, [&](auto tag) {
+        using T = decltype(tag);
+        if (plan.strategy == AR_ONESHOT)
+            return ar::launch_fused_oneshot<T>(a, packed, plan.shape, s);
+        return ar::launch_fused_twoshot<T>(a, packed, s);
+    }));
+}
+
+int ar_allreduce(const ar_params* p, int fusion_op, int strategy, ar_stream_t stream)
+{
+    if (p == nullptr)
+        return AR_ERR_INVALID_ARG;
+    if (fusion_op == AR_FUSION_NONE)
+        return ar_sum(p->partials, p->R, p->out, p->n, p->dtype, strategy, stream);
+    if (fusion_op != AR_FUSION_RESIDUAL_RMS_NORM)
+        return AR_ERR_UNSUPPORTED;
+    if (p->hidden < 1 || p->n % static_cast<size_t>(p->hidden) != 0 ||
+        p->n / static_cast<size_t>(p->hidden) > static_cast<size_t>(INT32_MAX))
+        return AR_ERR_INVALID_ARG;
+    const int tokens = static_cast<int>(p->n / static_cast<size_t>(p->hidden));
+    return ar_residual_rmsnorm(p->partials, p->R, p->bias, p->residual, p->weight, p->eps,
+                               p->hidden, tokens, p->out, p->residual_out, p->workspace,
+                               p->workspace_bytes, p->dtype, strategy, stream);
+}
+
+int ar_query_strategy(int R, size_t n, int hidden, int dtype, int fusion_op, int* chosen,
+                      int* warps_per_token)
+{
+    if (R < 1 || R > AR_MAX_RANKS || chosen == nullptr)
+        return AR_ERR_INVALID_ARG;
+    const int esize = esize_of(dtype);
+    if (esize == 0)
+        return AR_ERR_UNSUPPORTED;
+    if (fusion_op == AR_FUSION_NONE) {
+        *chosen = AR_ONESHOT;
+        if (warps_per_token)
+            *warps_per_token = 0;
+        return AR_OK;
+    }
+    if (fusion_op != AR_FUSION_RESIDUAL_RMS_NORM)
+        return AR_ERR_UNSUPPORTED;
+    if (hidden < 1 || n % static_cast<size_t>(hidden) != 0 ||
+        n / static_cast<size_t>(hidden) > static_cast<size_t>(INT32_MAX))
+        return AR_ERR_INVALID_ARG;
+    const int tokens = static_cast<int>(n / static_cast<size_t>(hidden));
+    const bool packed = hidden % (16 / esize) == 0;
+    FusedPlan plan = plan_fused(esize, R, hidden, tokens, packed, AR_AUTO);
+    *chosen = plan.strategy;
+    if (warps_per_token)
+        *warps_per_token = plan.strategy == AR_ONESHOT ? (plan.shape.tpr + 31) / 32 : 0;
+    return AR_OK;
+}
+
+}  // extern "C"

@@ -29,6 +29,14 @@ constexpr int kMaxVPTVec = 8;
 constexpr int kMaxVPTScalar = 16;
 constexpr int kMaxTPR = 1024;
 
+// Largest block of the one-shot fused kernel for a given units-per-thread:
+// more units per thread need more registers (VPT * lanes fp32 values of the
+// row stay live across the row reduction), so fewer threads per block.
+__host__ __device__ constexpr int oneshot_max_threads(int vpt)
+{
+    return vpt <= 2 ? 1024 : (vpt <= 8 ? 512 : 256);
+}
+
 struct SumArgs {
     const void* partials[kMaxRanks];
     void* out;

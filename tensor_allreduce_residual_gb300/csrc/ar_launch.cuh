@@ -1,0 +1,123 @@
+// ar_launch.cuh -- launchers: pick the compile-time specialisation (rank
+// count, units per thread) and the grid, then launch on the caller's stream.
+// Included once per element type by ar_kern_{f32,f16,bf16}.cu.
+//
+// Specialisations: the rank count R is a template parameter for 1..8 on the
+// reduce-only path and for 1, 2, 4 and 8 on the fused paths (the rank counts
+// of a tensor-parallel node; other R use a runtime loop), after the
+// AllReduceDispatchType -> AllReduceDispatchRanksPerNode templates of
+// "allreduce.d2".
+#pragma once
+
+#include <climits>
+
+#include "ar_kernels.cuh"
+
+namespace ar {
+
+template <typename T, bool PACKED, int R_CT, int UNROLL>
+static cudaError_t run_sum(const SumArgs& a, int nslices, cudaStream_t s)
+{
+    const uint64_t per_block = static_cast<uint64_t>(kFlatThreads) * UNROLL;
+    uint64_t gx = (a.slice + per_block - 1) / per_block;
+    if (gx == 0)
+        gx = 1;  // a tail-only launch still needs one block
+    if (gx > static_cast<uint64_t>(INT_MAX))
+        return cudaErrorInvalidConfiguration;
+    dim3 grid(static_cast<unsigned>(gx), static_cast<unsigned>(nslices));
+    k_sum<T, PACKED, R_CT, UNROLL><<<grid, kFlatThreads, 0, s>>>(a);
+    return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t launch_sum(const SumArgs& a, bool packed, int nslices, cudaStream_t s)
+{
+    if (!packed)
+        return run_sum<T, false, 0, 4>(a, nslices, s);
+    switch (a.R) {
+    case 1: return run_sum<T, true, 1, 8>(a, nslices, s);
+    case 2: return run_sum<T, true, 2, 8>(a, nslices, s);
+    case 3: return run_sum<T, true, 3, 4>(a, nslices, s);
+    case 4: return run_sum<T, true, 4, 4>(a, nslices, s);
+    case 5: return run_sum<T, true, 5, 2>(a, nslices, s);
+    case 6: return run_sum<T, true, 6, 2>(a, nslices, s);
+    case 7: return run_sum<T, true, 7, 2>(a, nslices, s);
+    case 8: return run_sum<T, true, 8, 2>(a, nslices, s);
+    default: return run_sum<T, true, 0, 2>(a, nslices, s);
+    }
+}
+
+template <typename T, bool PACKED, int R_CT, int VPT>
+static cudaError_t run_oneshot(const FusedArgs& a, OneShotShape sh, cudaStream_t s)
+{
+    const int threads = sh.tpr * sh.rows;
+    const unsigned grid = static_cast<unsigned>((a.tokens + sh.rows - 1) / sh.rows);
+    k_fused_oneshot<T, PACKED, R_CT, VPT><<<grid, threads, 0, s>>>(a, sh.tpr);
+    return cudaGetLastError();
+}
+
+template <typename T, bool PACKED, int R_CT>
+static cudaError_t oneshot_vpt(const FusedArgs& a, OneShotShape sh, cudaStream_t s)
+{
+    switch (sh.vpt) {
+    case 1: return run_oneshot<T, PACKED, R_CT, 1>(a, sh, s);
+    case 2: return run_oneshot<T, PACKED, R_CT, 2>(a, sh, s);
+    case 4: return run_oneshot<T, PACKED, R_CT, 4>(a, sh, s);
+    case 8: return run_oneshot<T, PACKED, R_CT, 8>(a, sh, s);
+    case 16:
+        if constexpr (!PACKED)
+            return run_oneshot<T, PACKED, R_CT, 16>(a, sh, s);
+        return cudaErrorInvalidValue;
+    default: return cudaErrorInvalidValue;
+    }
+}
+
+template <typename T>
+cudaError_t launch_fused_oneshot(const FusedArgs& a, bool packed, OneShotShape sh, cudaStream_t s)
+{
+    if (!packed)
+        return oneshot_vpt<T, false, 0>(a, sh, s);
+    switch (a.R) {
+    case 1: return oneshot_vpt<T, true, 1>(a, sh, s);
+    case 2: return oneshot_vpt<T, true, 2>(a, sh, s);
+    case 4: return oneshot_vpt<T, true, 4>(a, sh, s);
+    case 8: return oneshot_vpt<T, true, 8>(a, sh, s);
+    default: return oneshot_vpt<T, true, 0>(a, sh, s);
+    }
+}
+
+template <typename T, bool PACKED, int R_CT>
+static cudaError_t run_twoshot(const FusedArgs& a, cudaStream_t s)
+{
+    const uint64_t blocks = static_cast<uint64_t>(a.tokens) * a.nchunk;
+    if (blocks > static_cast<uint64_t>(INT_MAX))
+        return cudaErrorInvalidConfiguration;
+    k_twoshot_phase1<T, PACKED, R_CT><<<static_cast<unsigned>(blocks), kFlatThreads, 0, s>>>(a);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess)
+        return e;
+    k_twoshot_phase2<T, PACKED><<<static_cast<unsigned>(blocks), kFlatThreads, 0, s>>>(a);
+    return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t launch_fused_twoshot(const FusedArgs& a, bool packed, cudaStream_t s)
+{
+    if (!packed)
+        return run_twoshot<T, false, 0>(a, s);
+    switch (a.R) {
+    case 1: return run_twoshot<T, true, 1>(a, s);
+    case 2: return run_twoshot<T, true, 2>(a, s);
+    case 4: return run_twoshot<T, true, 4>(a, s);
+    case 8: return run_twoshot<T, true, 8>(a, s);
+    default: return run_twoshot<T, true, 0>(a, s);
+    }
+}
+
+}  // namespace ar
+
+#define AR_INSTANTIATE_LAUNCHERS(T)                                                                   \
+    template cudaError_t ar::launch_sum<T>(const ar::SumArgs&, bool, int, cudaStream_t);              \
+    template cudaError_t ar::launch_fused_oneshot<T>(const ar::FusedArgs&, bool, ar::OneShotShape,    \
+                                                     cudaStream_t);                                   \
+    template cudaError_t ar::launch_fused_twoshot<T>(const ar::FusedArgs&, bool, cudaStream_t);

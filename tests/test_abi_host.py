@@ -1,0 +1,200 @@
+"""Host-only checks of the C-ABI library: it builds, loads and exports every
+function include/ar.h declares; argument errors come back as status codes
+before anything is launched; the ctypes mirror of ar_params matches the C
+layout; workspace sizes and the AUTO choice are what the header states.
+
+No test here reaches a kernel launch: every call below fails validation or is
+an empty no-op, so these run the same with or without a GPU.
+"""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+import tensor_allreduce_residual_gb300 as ar
+from tensor_allreduce_residual_gb300 import _build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "ar.h")
+FAKE = 0x10000  # never dereferenced: every call using it fails validation first
+
+
+@pytest.fixture(scope="module")
+def L():
+    _build.build()
+    return ar.lib()
+
+
+def _declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"^\s*(?:const\s+)?[A-Za-z_][\w\s\*]*?\b(ar_\w+)\s*\(", text, flags=re.M)
+    return sorted(set(names))
+
+
+def test_header_declares_the_expected_entry_points():
+    names = _declared_functions()
+    for want in ["ar_version", "ar_strerror", "ar_workspace_size", "ar_workspace_size_rows", "ar_sum",
+                 "ar_residual_rmsnorm", "ar_allreduce", "ar_query_strategy"]:
+        assert want in names, names
+
+
+def test_library_exports_every_declared_symbol(L):
+    for name in _declared_functions():
+        assert hasattr(L, name), f"libar.so does not export {name}"
+    nm = subprocess.run(["nm", "-D", "--defined-only", ar.LIB_PATH], capture_output=True, text=True)
+    if nm.returncode == 0:
+        exported = set(re.findall(r"\bT (ar_\w+)", nm.stdout))
+        assert set(_declared_functions()) <= exported
+
+
+def test_version_and_strerror(L):
+    assert ar.ar_version() == 10000
+    for code in (ar.AR_OK, ar.AR_ERR_INVALID_ARG, ar.AR_ERR_UNSUPPORTED, ar.AR_ERR_WORKSPACE, ar.AR_ERR_CUDA):
+        assert ar.ar_strerror(code) and ar.ar_strerror(code) != "unknown status code"
+    assert ar.ar_strerror(12345) == "unknown status code"
+
+
+def test_params_struct_layout_matches_c(tmp_path):
+    src = tmp_path / "layout.c"
+    src.write_text(f'''
+#include <stdio.h>
+#include <stddef.h>
+#include "{HEADER}"
+int main(void) {{
+  printf("%zu %zu %zu %zu %zu %zu %zu %zu %zu %zu %zu %zu %zu %zu\\n", sizeof(ar_params),
+    offsetof(ar_params, partials), offsetof(ar_params, R), offsetof(ar_params, dtype),
+    offsetof(ar_params, n), offsetof(ar_params, out), offsetof(ar_params, bias),
+    offsetof(ar_params, residual), offsetof(ar_params, weight), offsetof(ar_params, eps),
+    offsetof(ar_params, hidden), offsetof(ar_params, residual_out),
+    offsetof(ar_params, workspace), offsetof(ar_params, workspace_bytes));
+  return 0;
+}}''')
+    exe = tmp_path / "layout"
+    subprocess.run(["gcc", "-std=c11", str(src), "-o", str(exe)], check=True)
+    got = [int(v) for v in subprocess.run([str(exe)], capture_output=True, text=True, check=True).stdout.split()]
+    P = ar.ArParams
+    want = [ctypes.sizeof(P)] + [getattr(P, f).offset for f in
+                                 ("partials", "R", "dtype", "n", "out", "bias", "residual", "weight", "eps",
+                                  "hidden", "residual_out", "workspace", "workspace_bytes")]
+    assert got == want
+
+
+def _ptrs(n, value=FAKE):
+    arr = (ctypes.c_void_p * max(n, 1))()
+    for k in range(n):
+        arr[k] = value + 256 * k
+    return arr
+
+
+def _sum(L, R, n=1024, dtype=ar.AR_FP16, strategy=ar.AR_ONESHOT, ptrs=None, out=FAKE + 65536):
+    return L.ar_sum(ptrs if ptrs is not None else _ptrs(R), R, out, n, dtype, strategy, None)
+
+
+def test_sum_argument_errors(L):
+    assert _sum(L, 0) == ar.AR_ERR_INVALID_ARG
+    assert _sum(L, ar.AR_MAX_RANKS + 1) == ar.AR_ERR_INVALID_ARG
+    assert _sum(L, -3) == ar.AR_ERR_INVALID_ARG
+    assert _sum(L, 2, dtype=7) == ar.AR_ERR_UNSUPPORTED
+    assert _sum(L, 2, strategy=ar.AR_NCCL) == ar.AR_ERR_UNSUPPORTED
+    assert _sum(L, 2, strategy=9) == ar.AR_ERR_UNSUPPORTED
+    assert _sum(L, 2, out=None) == ar.AR_ERR_INVALID_ARG
+    bad = _ptrs(2)
+    bad[1] = None
+    assert _sum(L, 2, ptrs=bad) == ar.AR_ERR_INVALID_ARG
+    assert L.ar_sum(None, 2, FAKE, 16, ar.AR_FP16, ar.AR_ONESHOT, None) == ar.AR_ERR_INVALID_ARG
+
+
+def test_empty_and_in_place_passthrough_launch_nothing(L):
+    assert _sum(L, 2, n=0) == ar.AR_OK
+    assert _sum(L, 2, n=0, ptrs=_ptrs(2, 0), out=None) == ar.AR_OK
+    # R = 1 with out == partials[0]: the tpSize = 1 passthrough, in place
+    assert _sum(L, 1, n=4096, ptrs=_ptrs(1), out=FAKE) == ar.AR_OK
+
+
+def _fused(L, R=2, bias=FAKE + 1 << 20, residual=FAKE + 2 << 20, weight=FAKE + 3 << 20, eps=1e-6,
+           hidden=64, tokens=4, out=FAKE + 4 << 20, residual_out=FAKE + 5 << 20, ws=None, ws_bytes=0,
+           dtype=ar.AR_FP32, strategy=ar.AR_TWOSHOT, ptrs=None):
+    return L.ar_residual_rmsnorm(ptrs if ptrs is not None else _ptrs(R), R, bias, residual, weight,
+                                 ctypes.c_float(eps), hidden, tokens, out, residual_out, ws, ws_bytes,
+                                 dtype, strategy, None)
+
+
+def test_fused_argument_errors(L):
+    assert _fused(L, R=0) == ar.AR_ERR_INVALID_ARG
+    assert _fused(L, R=17) == ar.AR_ERR_INVALID_ARG
+    assert _fused(L, hidden=0) == ar.AR_ERR_INVALID_ARG
+    assert _fused(L, tokens=-1) == ar.AR_ERR_INVALID_ARG
+    assert _fused(L, eps=-1e-6) == ar.AR_ERR_INVALID_ARG
+    assert _fused(L, eps=float("nan")) == ar.AR_ERR_INVALID_ARG
+    assert _fused(L, eps=float("inf")) == ar.AR_ERR_INVALID_ARG
+    assert _fused(L, residual=None) == ar.AR_ERR_INVALID_ARG
+    assert _fused(L, weight=None) == ar.AR_ERR_INVALID_ARG
+    assert _fused(L, out=None) == ar.AR_ERR_INVALID_ARG
+    assert _fused(L, residual_out=None) == ar.AR_ERR_INVALID_ARG
+    assert _fused(L, out=FAKE + 4 << 20, residual_out=FAKE + 4 << 20) == ar.AR_ERR_INVALID_ARG
+    assert _fused(L, dtype=5) == ar.AR_ERR_UNSUPPORTED
+    assert _fused(L, strategy=ar.AR_NCCL) == ar.AR_ERR_UNSUPPORTED
+    bad = _ptrs(2)
+    bad[0] = None
+    assert _fused(L, ptrs=bad) == ar.AR_ERR_INVALID_ARG
+
+
+def test_twoshot_workspace_errors(L):
+    need = L.ar_workspace_size_rows(2, 64, 4, ar.AR_FP32)
+    assert need > 0
+    assert _fused(L, strategy=ar.AR_TWOSHOT, ws=None) == ar.AR_ERR_WORKSPACE
+    assert _fused(L, strategy=ar.AR_TWOSHOT, ws=FAKE + 6 << 20, ws_bytes=0) == ar.AR_ERR_WORKSPACE
+    assert _fused(L, strategy=ar.AR_TWOSHOT, ws=FAKE + (6 << 20) + 2, ws_bytes=need) == ar.AR_ERR_WORKSPACE
+    # a row too long for the one-shot kernel: ONESHOT is unsupported, AUTO needs a workspace
+    long_row = 8 * 4096 * 2  # fp32 lanes * units per thread * threads, beyond the register budget
+    assert _fused(L, hidden=long_row, strategy=ar.AR_ONESHOT) == ar.AR_ERR_UNSUPPORTED
+    assert _fused(L, hidden=long_row, strategy=ar.AR_AUTO) == ar.AR_ERR_WORKSPACE
+
+
+def test_fused_empty_is_noop(L):
+    assert _fused(L, tokens=0, strategy=ar.AR_TWOSHOT) == ar.AR_OK
+    assert _fused(L, tokens=0, residual=None, out=None, residual_out=None, ptrs=_ptrs(2, 0)) == ar.AR_OK
+
+
+def test_allreduce_dispatch_errors(L):
+    assert L.ar_allreduce(None, 0, ar.AR_ONESHOT, None) == ar.AR_ERR_INVALID_ARG
+    p = ar.ArParams()
+    p.R, p.dtype, p.n = 2, ar.AR_FP16, 0
+    assert L.ar_allreduce(ctypes.byref(p), ar.AR_FUSION_NONE, ar.AR_ONESHOT, None) == ar.AR_OK
+    assert L.ar_allreduce(ctypes.byref(p), 7, ar.AR_ONESHOT, None) == ar.AR_ERR_UNSUPPORTED
+    p.n, p.hidden = 100, 64   # not a whole number of rows
+    assert L.ar_allreduce(ctypes.byref(p), ar.AR_FUSION_RESIDUAL_RMS_NORM, ar.AR_ONESHOT, None) == ar.AR_ERR_INVALID_ARG
+    p.hidden = 0
+    assert L.ar_allreduce(ctypes.byref(p), ar.AR_FUSION_RESIDUAL_RMS_NORM, ar.AR_ONESHOT, None) == ar.AR_ERR_INVALID_ARG
+
+
+def test_workspace_sizes(L):
+    assert L.ar_workspace_size(0, 100, ar.AR_FP16) == 0
+    assert L.ar_workspace_size(2, 0, ar.AR_FP16) == 0
+    assert L.ar_workspace_size(2, 100, 9) == 0
+    assert L.ar_workspace_size(2, 100, ar.AR_FP16) == 512        # 4 bytes per element, rounded to 256
+    for R, H, T, dt in [(8, 8192, 8192, ar.AR_BF16), (2, 4096, 32, ar.AR_FP16), (2, 64, 4, ar.AR_FP32),
+                        (3, 100, 7, ar.AR_FP16), (1, 1, 5, ar.AR_FP32)]:
+        rows = L.ar_workspace_size_rows(R, H, T, dt)
+        assert rows % 256 == 0 and rows >= T * 4
+        assert rows <= L.ar_workspace_size(R, H * T, dt)             # the bound covers every shape
+    assert L.ar_workspace_size_rows(8, 8192, 8192, ar.AR_BF16) == 8192 * 16 * 4
+    assert L.ar_workspace_size_rows(2, 0, 4, ar.AR_FP32) == 0
+
+
+def test_query_strategy(L):
+    s, w = ar.ar_query_strategy(4, 1 << 20, 0, ar.AR_FP16, ar.AR_FUSION_NONE)
+    assert s == ar.AR_ONESHOT and w == 0
+    s, w = ar.ar_query_strategy(2, 4096, 4096, ar.AR_FP16)          # TP decode, one token
+    assert s == ar.AR_ONESHOT and w >= 1
+    s, w = ar.ar_query_strategy(8, 64 * 8192, 8192, ar.AR_BF16)     # R=8 small prefill
+    assert s in (ar.AR_ONESHOT, ar.AR_TWOSHOT)
+    s, w = ar.ar_query_strategy(2, 4 * 65536 * 2, 65536 * 2, ar.AR_FP32)   # row beyond the one-shot budget
+    assert s == ar.AR_TWOSHOT and w == 0
+    with pytest.raises(ar.ARError):
+        ar.ar_query_strategy(2, 100, 64, ar.AR_FP32)                 # not a whole number of rows
+    with pytest.raises(ar.ARError):
+        ar.ar_query_strategy(0, 100, 10, ar.AR_FP32)

@@ -35,24 +35,27 @@ ELEM_SIZE = {"fp32": 4, "fp16": 2, "bf16": 2}
 K_RESIDUAL, K_BIAS, K_WEIGHT = 100, 200, 300
 
 
-def _gen(seed: int, k: int) -> torch.Generator:
-    g = torch.Generator(device="cpu")
+def _gen(seed: int, k: int, device: str = "cpu") -> torch.Generator:
+    g = torch.Generator(device=device)
     g.manual_seed(seed * 1000 + k)
     return g
 
 
-def draw(dist: tuple, numel: int, dtype: str, seed: int, k: int) -> torch.Tensor:
+def draw(dist: tuple, numel: int, dtype: str, seed: int, k: int, device: str = "cpu") -> torch.Tensor:
     """Draw ``numel`` values from ``dist`` and convert them to ``dtype``.
 
-    ``dist`` is ("U", lo, hi) or ("N", mean, variance).
+    ``dist`` is ("U", lo, hi) or ("N", mean, variance).  With device="cuda"
+    the values come from torch's CUDA generator (same recipe and seeds, a
+    different random stream than the CPU one); the benchmark uses it to make
+    its 1.5 GB inputs quickly.
     """
-    g = _gen(seed, k)
+    g = _gen(seed, k, device)
     kind, a, b = dist
     if kind == "U":
-        v = torch.rand(numel, generator=g, dtype=torch.float32)
+        v = torch.rand(numel, generator=g, dtype=torch.float32, device=device)
         v.mul_(b - a).add_(a)
     elif kind == "N":
-        v = torch.randn(numel, generator=g, dtype=torch.float32)
+        v = torch.randn(numel, generator=g, dtype=torch.float32, device=device)
         v.mul_(math.sqrt(b)).add_(a)
     else:
         raise ValueError(f"unknown distribution {dist!r}")
@@ -81,19 +84,20 @@ class FusedInputs:
     extra: dict = field(default_factory=dict)
 
 
-def sum_inputs(R: int, n: int, dtype: str, dist=("U", -1.0, 1.0), seed: int = 0) -> SumInputs:
-    parts = [draw(dist, n, dtype, seed, r) for r in range(R)]
+def sum_inputs(R: int, n: int, dtype: str, dist=("U", -1.0, 1.0), seed: int = 0,
+               device: str = "cpu") -> SumInputs:
+    parts = [draw(dist, n, dtype, seed, r, device) for r in range(R)]
     return SumInputs(R, n, dtype, parts)
 
 
 def fused_inputs(R: int, tokens: int, hidden: int, dtype: str, *,
                  partial_dist, residual_dist, weight_dist, bias_dist=None,
-                 eps: float, seed: int = 0) -> FusedInputs:
+                 eps: float, seed: int = 0, device: str = "cpu") -> FusedInputs:
     n = tokens * hidden
-    parts = [draw(partial_dist, n, dtype, seed, r).view(tokens, hidden) for r in range(R)]
-    residual = draw(residual_dist, n, dtype, seed, K_RESIDUAL).view(tokens, hidden)
-    weight = draw(weight_dist, hidden, dtype, seed, K_WEIGHT)
-    bias = None if bias_dist is None else draw(bias_dist, hidden, dtype, seed, K_BIAS)
+    parts = [draw(partial_dist, n, dtype, seed, r, device).view(tokens, hidden) for r in range(R)]
+    residual = draw(residual_dist, n, dtype, seed, K_RESIDUAL, device).view(tokens, hidden)
+    weight = draw(weight_dist, hidden, dtype, seed, K_WEIGHT, device)
+    bias = None if bias_dist is None else draw(bias_dist, hidden, dtype, seed, K_BIAS, device)
     return FusedInputs(R, tokens, hidden, dtype, eps, parts, residual, weight, bias)
 
 
@@ -108,33 +112,33 @@ def pr1(seed: int = 0) -> FusedInputs:
                         weight_dist=("N", 1.0, 0.1), eps=1e-6, seed=seed)
 
 
-def tp_decode(tokens: int, seed: int = 0) -> FusedInputs:
+def tp_decode(tokens: int, seed: int = 0, device: str = "cpu") -> FusedInputs:
     """R=2 fp16, H=4096; partials N(0,1/2), residual N(0,4), bias N(0,0.02), w N(1,0.05), eps=1e-5."""
     R = 2
     return fused_inputs(R, tokens, 4096, "fp16", partial_dist=("N", 0.0, 1.0 / R),
                         residual_dist=("N", 0.0, 4.0), bias_dist=("N", 0.0, 0.02),
-                        weight_dist=("N", 1.0, 0.05), eps=1e-5, seed=seed)
+                        weight_dist=("N", 1.0, 0.05), eps=1e-5, seed=seed, device=device)
 
 
-def decode_r8(tokens: int, seed: int = 0) -> FusedInputs:
+def decode_r8(tokens: int, seed: int = 0, device: str = "cpu") -> FusedInputs:
     """R=8 bf16, H=8192; partials N(0,1/8), residual N(0,4), no bias, w N(1,0.05), eps=1e-6."""
     R = 8
     return fused_inputs(R, tokens, 8192, "bf16", partial_dist=("N", 0.0, 1.0 / R),
                         residual_dist=("N", 0.0, 4.0), bias_dist=None,
-                        weight_dist=("N", 1.0, 0.05), eps=1e-6, seed=seed)
+                        weight_dist=("N", 1.0, 0.05), eps=1e-6, seed=seed, device=device)
 
 
-def reduce_only(n: int, seed: int = 0) -> SumInputs:
+def reduce_only(n: int, seed: int = 0, device: str = "cpu") -> SumInputs:
     """R=4 fp16, flat n elements, partials U(-1,1)."""
-    return sum_inputs(4, n, "fp16", ("U", -1.0, 1.0), seed)
+    return sum_inputs(4, n, "fp16", ("U", -1.0, 1.0), seed, device)
 
 
-def tp_prefill(tokens: int = 8192, hidden: int = 8192, seed: int = 0) -> FusedInputs:
+def tp_prefill(tokens: int = 8192, hidden: int = 8192, seed: int = 0, device: str = "cpu") -> FusedInputs:
     """R=8 bf16, T=8192, H=8192; partials N(0,1/8), residual N(0,4), bias N(0,0.02), w N(1,0.05), eps=1e-6."""
     R = 8
     return fused_inputs(R, tokens, hidden, "bf16", partial_dist=("N", 0.0, 1.0 / R),
                         residual_dist=("N", 0.0, 4.0), bias_dist=("N", 0.0, 0.02),
-                        weight_dist=("N", 1.0, 0.05), eps=1e-6, seed=seed)
+                        weight_dist=("N", 1.0, 0.05), eps=1e-6, seed=seed, device=device)
 
 
 TP_DECODE_TOKENS = list(range(1, 33))
