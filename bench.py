@@ -49,6 +49,7 @@ def parse_args():
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--strategy", default="AUTO", choices=["AUTO", "ONESHOT", "TWOSHOT"])
     p.add_argument("--e2e-steps", type=int, default=10)
+    p.add_argument("--tokens", type=int, default=TOKENS, help="token rows per GPU (default: the workload's 8192)")
     p.add_argument("--no-extras", action="store_true", help="skip the secondary workloads")
     p.add_argument("--no-cpu-baseline", action="store_true")
     return p.parse_args()
@@ -165,6 +166,8 @@ class ClockSampler:
 # ----------------------------------------------------------------------------- our arm
 
 def run_ours(args, rank, world, local_rank):
+    global TOKENS
+    TOKENS = args.tokens
     import torch
     import torch.distributed as dist
 
@@ -278,11 +281,11 @@ def run_ours(args, rank, world, local_rank):
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms_step, 5), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": DATA,
-        "config": {"workload": WORKLOAD, "R": R, "tokens_per_gpu": TOKENS, "global_tokens": TOKENS * world,
+        "config": {"workload": WORKLOAD.replace("tokens=8192", f"tokens={TOKENS}"), "R": R, "tokens_per_gpu": TOKENS, "global_tokens": TOKENS * world,
                    "hidden": HIDDEN, "io_dtype": "bf16", "eps": EPS, "strategy": args.strategy,
                    "resolved_strategy": resolved, "warps_per_token": warps,
                    "bytes_per_call": bytes_call, "parallelism": f"rows sharded over {world} GPU(s), no collective",
-                   "l2": "inputs larger than L2 (1.48 GB per call vs 129 MB L2): no flush between steps"},
+                   "l2": f"inputs larger than L2 ({bytes_call / 1e9:.2f} GB per call vs 129 MB L2): no flush between steps"},
         "us_per_call": round(ms_step * 1e3, 2), "frac_of_peak": round(value / world / peak, 4),
         "clocks": clocks, "e2e": e2e, "gpu_launches": launches_per_step * args.steps, "roofline": roofline,
     }
@@ -411,7 +414,7 @@ def run_reference(args, rank, world):
         "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": DATA,
-        "config": {"workload": WORKLOAD, "R": R, "tokens_per_gpu": TOKENS, "hidden": HIDDEN, "io_dtype": "bf16",
+        "config": {"workload": WORKLOAD.replace("tokens=8192", f"tokens={TOKENS}"), "R": R, "tokens_per_gpu": TOKENS, "hidden": HIDDEN, "io_dtype": "bf16",
                    "eps": EPS, "sample_rows_per_step": rows},
         "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
                          "sample": f"{rows} rows of the workload per step, single-threaded binary64 C oracle"},

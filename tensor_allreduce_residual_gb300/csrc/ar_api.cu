@@ -8,6 +8,8 @@
 
 #include <cmath>
 #include <cstdint>
+#include <cstdio>
+#include <cstdlib>
 
 #include "ar.h"
 #include "ar_auto_table.h"
@@ -63,34 +65,50 @@ int next_pow2(int v)
 
 // ---------------------------------------------------------------- one-shot shape
 
-// Threads per row = units_row / vpt rounded up to a power of two, at most
-// kMaxTPR; blocks hold at least 128 threads.  Returns false when the row does
-// not fit in registers (then only the two-shot path can take it).
-bool oneshot_shape(int units_row, int vpt, bool packed, OneShotShape* sh)
+// Threads per row = units_row / vpt rounded up to a power of two; blocks hold
+// at least 128 threads.  Register-resident rows are limited by the registers
+// a thread may use, staged rows by shared memory.  Returns false when the
+// row does not fit (then only the two-shot path can take it).
+bool oneshot_shape(int units_row, int vpt, int lanes, bool packed, int mode, int R, OneShotShape* sh)
 {
     const int max_vpt = packed ? ar::kMaxVPTVec : ar::kMaxVPTScalar;
-    if (vpt < 1 || vpt > max_vpt)
+    const bool stage = mode != ar::kRegisters;
+    if (vpt < 1 || vpt > max_vpt || (stage && (!packed || vpt > ar::kMaxVPTVec)))
         return false;
     const int tpr = next_pow2((units_row + vpt - 1) / vpt);
-    if (tpr > ar::kMaxTPR || tpr > ar::oneshot_max_threads(vpt))
+    const int max_threads = stage ? ar::kMaxTPR : ar::oneshot_max_threads(vpt * lanes);
+    if (tpr > ar::kMaxTPR || tpr > max_threads)
         return false;
+    // The persistent form needs whole-warp rows and R known at compile time.
+    if (mode == ar::kPersistent &&
+        (tpr < 128 || tpr > ar::kMaxPersistThreads || !(R == 1 || R == 2 || R == 4 || R == 8)))
+        mode = ar::kStaged;
     sh->tpr = tpr;
     sh->vpt = vpt;
     sh->rows = tpr >= 128 ? 1 : 128 / tpr;
+    sh->mode = mode;
+    sh->smem_bytes = 0;
+    if (stage) {
+        const size_t bytes = static_cast<size_t>(sh->rows) * lanes * units_row * sizeof(float);
+        if (bytes > static_cast<size_t>(ar::kMaxStageBytes))
+            return false;
+        sh->smem_bytes = static_cast<int>(bytes);
+    }
     return true;
 }
 
 // Rule used when the measured table has no entry: aim for 512 threads per
 // row when there are few rows (more memory parallelism per row) and 256
 // otherwise, with the smallest units-per-thread that reaches it.
-int rule_vpt(int units_row, int tokens, bool packed)
+int rule_vpt(int units_row, int tokens, int lanes, bool packed)
 {
     const int max_vpt = packed ? ar::kMaxVPTVec : ar::kMaxVPTScalar;
     const int target = tokens <= 32 ? 512 : 256;
     int vpt = 1;
     while (vpt < max_vpt && (units_row + vpt - 1) / vpt > target)
         vpt <<= 1;
-    while (vpt < max_vpt && next_pow2((units_row + vpt - 1) / vpt) > ar::oneshot_max_threads(vpt))
+    while (vpt < max_vpt &&
+           next_pow2((units_row + vpt - 1) / vpt) > ar::oneshot_max_threads(vpt * lanes))
         vpt <<= 1;
     return vpt;
 }
@@ -106,6 +124,34 @@ const ar::AutoEntry* table_lookup(int esize, int R, int units_row, int tokens)
     return nullptr;
 }
 
+// Measurement override of the one-shot shape: AR_ONESHOT_SHAPE="vpt:mode" or
+// "vpt:mode:early" (e.g. "4:1" or "2:0:1") replaces the table and the rule
+// for every packed call.  Read once per process; used to sweep shapes when
+// building the AUTO table.
+struct ShapeOverride {
+    int vpt = 0;
+    int mode = 0;
+    int early = 0;
+};
+
+const ShapeOverride& shape_override()
+{
+    static const ShapeOverride ov = [] {
+        ShapeOverride o;
+        if (const char* env = std::getenv("AR_ONESHOT_SHAPE")) {
+            int v = 0, st = 0, early = 0;
+            const int got = std::sscanf(env, "%d:%d:%d", &v, &st, &early);
+            if (got >= 2 && v > 0 && st >= 0 && st <= 2) {
+                o.vpt = v;
+                o.mode = st;
+                o.early = got == 3 && early != 0;
+            }
+        }
+        return o;
+    }();
+    return ov;
+}
+
 struct FusedPlan {
     int strategy;      // AR_ONESHOT or AR_TWOSHOT
     bool oneshot_ok;   // the row fits the one-shot kernel
@@ -115,19 +161,34 @@ struct FusedPlan {
 // Resolves AUTO and the one-shot shape for a fused call.
 FusedPlan plan_fused(int esize, int R, int hidden, int tokens, bool packed, int strategy)
 {
-    const int lanes = 16 / esize;
-    const int units_row = packed ? hidden / lanes : hidden;
+    const int lanes = packed ? 16 / esize : 1;
+    const int units_row = hidden / lanes;
     FusedPlan p{};
-    int vpt = rule_vpt(units_row, tokens, packed);
+    int vpt = rule_vpt(units_row, tokens, lanes, packed);
+    int mode = ar::kRegisters;
+    int early = 1;
     int auto_strategy = AR_ONESHOT;
     if (packed) {
         if (const ar::AutoEntry* e = table_lookup(esize, R, units_row, tokens)) {
             auto_strategy = e->strategy;
-            if (e->vpt > 0)
+            if (e->vpt > 0) {
                 vpt = e->vpt;
+                mode = e->mode;
+                early = e->early;
+            }
+        }
+        const ShapeOverride& ov = shape_override();
+        if (ov.vpt > 0) {
+            vpt = ov.vpt;
+            mode = ov.mode;
+            early = ov.early;
         }
     }
-    p.oneshot_ok = oneshot_shape(units_row, vpt, packed, &p.shape);
+    p.oneshot_ok = oneshot_shape(units_row, vpt, lanes, packed, mode, R, &p.shape);
+    if (!p.oneshot_ok)  // the chosen shape does not fit this row: the rule's shape
+        p.oneshot_ok = oneshot_shape(units_row, rule_vpt(units_row, tokens, lanes, packed), lanes,
+                                     packed, ar::kRegisters, R, &p.shape);
+    p.shape.early_residual = early;
     if (!p.oneshot_ok)
         auto_strategy = AR_TWOSHOT;
     p.strategy = strategy == AR_AUTO ? auto_strategy : strategy;
@@ -286,6 +347,7 @@ int ar_residual_rmsnorm(const void* const* partials, int R, const void* bias, co
     a.nchunk = nchunk;
     a.chunk_units = ar::kFlatThreads * ar::kChunkVPT;
     a.eps = eps;
+    a.early_residual = plan.shape.early_residual;
 
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     return status_of(by_dtype(dtype, [&](auto tag) {

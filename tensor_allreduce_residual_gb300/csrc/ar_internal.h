@@ -29,12 +29,13 @@ constexpr int kMaxVPTVec = 8;
 constexpr int kMaxVPTScalar = 16;
 constexpr int kMaxTPR = 1024;
 
-// Largest block of the one-shot fused kernel for a given units-per-thread:
-// more units per thread need more registers (VPT * lanes fp32 values of the
-// row stay live across the row reduction), so fewer threads per block.
-__host__ __device__ constexpr int oneshot_max_threads(int vpt)
+// Largest block of the one-shot fused kernel for a thread that holds
+// `values` fp32 values of its row (units per thread * lanes per unit): they
+// stay live across the row reduction, so more values need more registers
+// per thread and hence fewer threads per block.
+__host__ __device__ constexpr int oneshot_max_threads(int values)
 {
-    return vpt <= 2 ? 1024 : (vpt <= 8 ? 512 : 256);
+    return values <= 16 ? 1024 : (values <= 32 ? 512 : 256);
 }
 
 struct SumArgs {
@@ -61,15 +62,35 @@ struct FusedArgs {
     int nchunk;            // two-shot chunks per row
     int chunk_units;       // two-shot units per chunk
     float eps;
+    int early_residual;    // one-shot: write residual_out before the row barrier
+};
+
+// Where the one-shot fused kernel keeps a row's fp32 sums between the sum and
+// the normalisation.
+enum OneShotMode {
+    kRegisters = 0,   // registers, one block per `rows` rows
+    kStaged = 1,      // shared memory, one block per `rows` rows
+    kPersistent = 2   // shared memory, persistent blocks striding over rows
 };
 
 // One-shot fused launch shape: `tpr` threads per row (a power of two),
-// `vpt` units per thread, `rows` rows per block.
+// `vpt` units per thread, `rows` rows per block, the mode, the dynamic
+// shared memory of the staged modes, and when residual_out is written.
 struct OneShotShape {
     int tpr;
     int vpt;
     int rows;
+    int mode;
+    int smem_bytes;
+    int early_residual;  // write residual_out before the row barrier
 };
+
+// Largest block of the persistent one-shot kernel (it keeps the next row's
+// first units in registers across the row barrier, so it needs more of them).
+constexpr int kMaxPersistThreads = 512;
+
+// Largest dynamic shared memory a staged one-shot block may use.
+constexpr int kMaxStageBytes = 96 * 1024;
 
 // Launchers, explicitly instantiated for float, __half and __nv_bfloat16 in
 // the per-dtype translation units.  Each returns the cudaError_t of the launch.

@@ -19,6 +19,10 @@
 
 #include "ar_internal.h"
 
+#ifndef AR_L2_PREFETCH_256B
+#define AR_L2_PREFETCH_256B 0
+#endif
+
 namespace ar {
 
 // ---------------------------------------------------------------------------
@@ -30,9 +34,15 @@ namespace ar {
 __device__ __forceinline__ uint4 ld_stream16(const void* p)
 {
     uint4 r;
+#if AR_L2_PREFETCH_256B
+    asm("ld.global.nc.L1::no_allocate.L2::256B.v4.u32 {%0, %1, %2, %3}, [%4];"
+        : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+        : "l"(p));
+#else
     asm("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
         : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
         : "l"(p));
+#endif
     return r;
 }
 
@@ -323,45 +333,66 @@ __device__ __forceinline__ float inv_rms(float sumsq, int hidden, float eps)
 // (one_shot_all_reduce_norm_kernel -> rms_norm, "allreduce.d2").
 //
 // `tpr` threads (a power of two, = 32 * warps per token when >= 32) own one
-// row; each keeps VPT units of the row in fp32 registers between the sum and
-// the normalisation, so every input byte is read from HBM once and every
-// output byte written once.  Blocks hold blockDim.x / tpr rows.
+// row; each handles VPT units of it and keeps their fp32 sums x on chip
+// between the sum and the normalisation -- in registers (STAGE = false) or
+// in shared memory (STAGE = true, which frees the registers for more rows in
+// flight per SM).  Either way every input byte is read from HBM once and
+// every output byte written once.  residual_out does not depend on the norm:
+// with EARLY it is written as soon as x is known (spreading the row's writes
+// over its reads), otherwise together with `out` after the row barrier.
+// Which order keeps HBM busier depends on the shape (and it changes how the
+// compiler schedules the loads), so both are compiled and the launch shape
+// picks one.  Blocks hold blockDim.x / tpr rows.
+// A thread reads back from shared memory only the values it wrote itself,
+// so staging needs no barrier of its own.
 // ---------------------------------------------------------------------------
-template <typename T, bool PACKED, int R_CT, int VPT>
-__global__ void __launch_bounds__(oneshot_max_threads(VPT))
+template <typename T, bool PACKED, int R_CT, int VPT, bool STAGE, bool EARLY>
+__global__ void __launch_bounds__(STAGE ? 1024 : oneshot_max_threads(VPT * Unit<T, PACKED>::L))
 k_fused_oneshot(const FusedArgs a, const int tpr)
 {
     using U = Unit<T, PACKED>;
     constexpr int L = U::L;
     __shared__ float red[32];
+    extern __shared__ float xs_all[];  // STAGE: [rows per block][L][units_row] fp32
 
     const int lane_row = threadIdx.x & (tpr - 1);
-    const int row = blockIdx.x * (blockDim.x / tpr) + threadIdx.x / tpr;
+    const int row_in_block = threadIdx.x / tpr;
+    const int row = blockIdx.x * (blockDim.x / tpr) + row_in_block;
     const bool row_ok = row < a.tokens;
     const uint64_t row_off = static_cast<uint64_t>(row) * a.units_row;
+    float* xs = xs_all + static_cast<size_t>(row_in_block) * L * a.units_row;
 
-    float x[VPT][L];
-    typename U::raw wv[VPT];
+    float x[STAGE ? 1 : VPT][L];
+    typename U::raw wv[STAGE ? 1 : VPT];
     float ss = 0.0f;
 #pragma unroll
     for (int k = 0; k < VPT; ++k) {
         const int j = lane_row + k * tpr;
+        float* xk = x[STAGE ? 0 : k];
 #pragma unroll
         for (int l = 0; l < L; ++l)
-            x[k][l] = 0.0f;
+            xk[l] = 0.0f;
         if (row_ok && j < a.units_row) {
-            sum_partials<T, PACKED, R_CT>(a.partials, a.R, row_off + j, x[k]);
+            sum_partials<T, PACKED, R_CT>(a.partials, a.R, row_off + j, xk);
             float t[L];
             if (a.bias != nullptr) {
                 U::to_float(U::load_cached(a.bias, j), t);
-                add_lanes<L>(x[k], t);
+                add_lanes<L>(xk, t);
             }
             U::to_float(U::load(a.residual, row_off + j), t);
-            add_lanes<L>(x[k], t);
-            wv[k] = U::load_cached(a.weight, j);
+            add_lanes<L>(xk, t);
+            if constexpr (!STAGE)
+                wv[k] = U::load_cached(a.weight, j);
+            if constexpr (EARLY)
+                U::store(a.residual_out, row_off + j, xk);
 #pragma unroll
             for (int l = 0; l < L; ++l)
-                ss = fmaf(x[k][l], x[k][l], ss);
+                ss = fmaf(xk[l], xk[l], ss);
+            if constexpr (STAGE) {
+#pragma unroll
+                for (int l = 0; l < L; ++l)
+                    xs[l * a.units_row + j] = xk[l];
+            }
         }
     }
 
@@ -372,13 +403,120 @@ k_fused_oneshot(const FusedArgs a, const int tpr)
     for (int k = 0; k < VPT; ++k) {
         const int j = lane_row + k * tpr;
         if (row_ok && j < a.units_row) {
-            U::store(a.residual_out, row_off + j, x[k]);
-            float w[L], y[L];
-            U::to_float(wv[k], w);
+            float xk[L], w[L], y[L];
+            if constexpr (STAGE) {
+#pragma unroll
+                for (int l = 0; l < L; ++l)
+                    xk[l] = xs[l * a.units_row + j];
+                U::to_float(U::load_cached(a.weight, j), w);
+            } else {
+#pragma unroll
+                for (int l = 0; l < L; ++l)
+                    xk[l] = x[k][l];
+                U::to_float(wv[k], w);
+            }
+            if constexpr (!EARLY)
+                U::store(a.residual_out, row_off + j, xk);
 #pragma unroll
             for (int l = 0; l < L; ++l)
-                y[l] = x[k][l] * inv * w[l];
+                y[l] = xk[l] * inv * w[l];
             U::store(a.out, row_off + j, y);
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// A4, persistent form for many rows: one row per block iteration, blocks
+// stride over the rows.  The row's fp32 sums are staged in shared memory; the
+// first units of the NEXT row (its partials and residual) are loaded before
+// the row-reduction barrier, so loads stay in flight while the block waits
+// at the barrier and writes the current row.  Packed path, R known at
+// compile time, tpr == blockDim.x.
+// ---------------------------------------------------------------------------
+template <typename T, int R_CT, int VPT>
+__global__ void __launch_bounds__(kMaxPersistThreads)
+k_fused_oneshot_persist(const FusedArgs a)
+{
+    using U = Unit<T, true>;
+    constexpr int L = U::L;
+    static_assert(R_CT > 0, "persistent one-shot needs R at compile time");
+    __shared__ float red[2][32];
+    extern __shared__ float xs[];  // [L][units_row] fp32
+
+    const int tpr = blockDim.x;
+    const int j0 = threadIdx.x;
+    const bool j0_ok = j0 < a.units_row;
+    uint4 pre[R_CT + 1];  // units j0 of the next row: R partials and the residual
+    int row = blockIdx.x;
+    if (row < a.tokens && j0_ok) {
+        const uint64_t off = static_cast<uint64_t>(row) * a.units_row + j0;
+#pragma unroll
+        for (int r = 0; r < R_CT; ++r)
+            pre[r] = U::load(a.partials[r], off);
+        pre[R_CT] = U::load(a.residual, off);
+    }
+    int parity = 0;
+    for (; row < a.tokens; row += gridDim.x, parity ^= 1) {
+        const uint64_t row_off = static_cast<uint64_t>(row) * a.units_row;
+        float ss = 0.0f;
+#pragma unroll
+        for (int k = 0; k < VPT; ++k) {
+            const int j = j0 + k * tpr;
+            if (j < a.units_row) {
+                float x[L], t[L];
+                if (k == 0) {
+                    U::to_float(pre[0], x);
+#pragma unroll
+                    for (int r = 1; r < R_CT; ++r) {
+                        U::to_float(pre[r], t);
+                        add_lanes<L>(x, t);
+                    }
+                } else {
+                    sum_partials<T, true, R_CT>(a.partials, R_CT, row_off + j, x);
+                }
+                if (a.bias != nullptr) {
+                    U::to_float(U::load_cached(a.bias, j), t);
+                    add_lanes<L>(x, t);
+                }
+                U::to_float(k == 0 ? pre[R_CT] : U::load(a.residual, row_off + j), t);
+                add_lanes<L>(x, t);
+                if (a.early_residual)
+                    U::store(a.residual_out, row_off + j, x);
+#pragma unroll
+                for (int l = 0; l < L; ++l) {
+                    ss = fmaf(x[l], x[l], ss);
+                    xs[l * a.units_row + j] = x[l];
+                }
+            }
+        }
+        const int next = row + gridDim.x;
+        if (next < a.tokens && j0_ok) {
+            const uint64_t off = static_cast<uint64_t>(next) * a.units_row + j0;
+#pragma unroll
+            for (int r = 0; r < R_CT; ++r)
+                pre[r] = U::load(a.partials[r], off);
+            pre[R_CT] = U::load(a.residual, off);
+        }
+        // Row reduction with a double-buffered scratch: a warp that runs ahead
+        // into the next row writes the other buffer.
+        ss = row_sum(ss, tpr, red[parity]);
+        const float inv = inv_rms(ss, a.hidden, a.eps);
+#pragma unroll
+        for (int k = 0; k < VPT; ++k) {
+            const int j = j0 + k * tpr;
+            if (j < a.units_row) {
+                float x[L], w[L], y[L];
+#pragma unroll
+                for (int l = 0; l < L; ++l)
+                    x[l] = xs[l * a.units_row + j];
+                U::to_float(U::load_cached(a.weight, j), w);
+                if (!a.early_residual)
+                    U::store(a.residual_out, row_off + j, x);
+#pragma unroll
+                for (int l = 0; l < L; ++l)
+                    y[l] = x[l] * inv * w[l];
+                U::store(a.out, row_off + j, y);
+            }
         }
     }
 }

@@ -47,42 +47,99 @@ cudaError_t launch_sum(const SumArgs& a, bool packed, int nslices, cudaStream_t 
     }
 }
 
-template <typename T, bool PACKED, int R_CT, int VPT>
+template <typename T, bool PACKED, int R_CT, int VPT, bool STAGE, bool EARLY>
 static cudaError_t run_oneshot(const FusedArgs& a, OneShotShape sh, cudaStream_t s)
 {
+    auto kernel = k_fused_oneshot<T, PACKED, R_CT, VPT, STAGE, EARLY>;
+    if (STAGE && sh.smem_bytes > 48 * 1024) {
+        // Beyond 48 KB of dynamic shared memory a kernel must opt in (per device).
+        const cudaError_t attr = cudaFuncSetAttribute(
+            kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxStageBytes);
+        if (attr != cudaSuccess)
+            return attr;
+    }
     const int threads = sh.tpr * sh.rows;
     const unsigned grid = static_cast<unsigned>((a.tokens + sh.rows - 1) / sh.rows);
-    k_fused_oneshot<T, PACKED, R_CT, VPT><<<grid, threads, 0, s>>>(a, sh.tpr);
+    kernel<<<grid, threads, STAGE ? sh.smem_bytes : 0, s>>>(a, sh.tpr);
     return cudaGetLastError();
 }
 
-template <typename T, bool PACKED, int R_CT>
+template <typename T, bool PACKED, int R_CT, bool STAGE, bool EARLY>
 static cudaError_t oneshot_vpt(const FusedArgs& a, OneShotShape sh, cudaStream_t s)
 {
     switch (sh.vpt) {
-    case 1: return run_oneshot<T, PACKED, R_CT, 1>(a, sh, s);
-    case 2: return run_oneshot<T, PACKED, R_CT, 2>(a, sh, s);
-    case 4: return run_oneshot<T, PACKED, R_CT, 4>(a, sh, s);
-    case 8: return run_oneshot<T, PACKED, R_CT, 8>(a, sh, s);
+    case 1: return run_oneshot<T, PACKED, R_CT, 1, STAGE, EARLY>(a, sh, s);
+    case 2: return run_oneshot<T, PACKED, R_CT, 2, STAGE, EARLY>(a, sh, s);
+    case 4: return run_oneshot<T, PACKED, R_CT, 4, STAGE, EARLY>(a, sh, s);
+    case 8: return run_oneshot<T, PACKED, R_CT, 8, STAGE, EARLY>(a, sh, s);
     case 16:
-        if constexpr (!PACKED)
-            return run_oneshot<T, PACKED, R_CT, 16>(a, sh, s);
+        if constexpr (!PACKED && !STAGE)
+            return run_oneshot<T, PACKED, R_CT, 16, STAGE, EARLY>(a, sh, s);
         return cudaErrorInvalidValue;
     default: return cudaErrorInvalidValue;
     }
+}
+
+template <typename T, bool PACKED, int R_CT, bool STAGE>
+static cudaError_t oneshot_order(const FusedArgs& a, OneShotShape sh, cudaStream_t s)
+{
+    return sh.early_residual ? oneshot_vpt<T, PACKED, R_CT, STAGE, true>(a, sh, s)
+                             : oneshot_vpt<T, PACKED, R_CT, STAGE, false>(a, sh, s);
+}
+
+template <typename T, int R_CT, int VPT>
+static cudaError_t run_persist(const FusedArgs& a, OneShotShape sh, cudaStream_t s)
+{
+    auto kernel = k_fused_oneshot_persist<T, R_CT, VPT>;
+    if (sh.smem_bytes > 48 * 1024) {
+        const cudaError_t attr = cudaFuncSetAttribute(
+            kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxStageBytes);
+        if (attr != cudaSuccess)
+            return attr;
+    }
+    int dev = 0, sms = 0, per_sm = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess)
+        e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e == cudaSuccess)
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, sh.tpr, sh.smem_bytes);
+    if (e != cudaSuccess)
+        return e;
+    const long long resident = static_cast<long long>(sms) * (per_sm > 0 ? per_sm : 1);
+    const unsigned grid = static_cast<unsigned>(a.tokens < resident ? a.tokens : resident);
+    kernel<<<grid, sh.tpr, sh.smem_bytes, s>>>(a);
+    return cudaGetLastError();
+}
+
+template <typename T, int R_CT>
+static cudaError_t oneshot_packed(const FusedArgs& a, OneShotShape sh, cudaStream_t s)
+{
+    if constexpr (R_CT > 0) {
+        if (sh.mode == kPersistent) {
+            switch (sh.vpt) {
+            case 1: return run_persist<T, R_CT, 1>(a, sh, s);
+            case 2: return run_persist<T, R_CT, 2>(a, sh, s);
+            case 4: return run_persist<T, R_CT, 4>(a, sh, s);
+            case 8: return run_persist<T, R_CT, 8>(a, sh, s);
+            default: return cudaErrorInvalidValue;
+            }
+        }
+    }
+    return sh.mode != kRegisters ? oneshot_order<T, true, R_CT, true>(a, sh, s)
+                                 : oneshot_order<T, true, R_CT, false>(a, sh, s);
 }
 
 template <typename T>
 cudaError_t launch_fused_oneshot(const FusedArgs& a, bool packed, OneShotShape sh, cudaStream_t s)
 {
     if (!packed)
-        return oneshot_vpt<T, false, 0>(a, sh, s);
+        return oneshot_vpt<T, false, 0, false, true>(a, sh, s);
     switch (a.R) {
-    case 1: return oneshot_vpt<T, true, 1>(a, sh, s);
-    case 2: return oneshot_vpt<T, true, 2>(a, sh, s);
-    case 4: return oneshot_vpt<T, true, 4>(a, sh, s);
-    case 8: return oneshot_vpt<T, true, 8>(a, sh, s);
-    default: return oneshot_vpt<T, true, 0>(a, sh, s);
+    case 1: return oneshot_packed<T, 1>(a, sh, s);
+    case 2: return oneshot_packed<T, 2>(a, sh, s);
+    case 4: return oneshot_packed<T, 4>(a, sh, s);
+    case 8: return oneshot_packed<T, 8>(a, sh, s);
+    default: return oneshot_packed<T, 0>(a, sh, s);
     }
 }
 

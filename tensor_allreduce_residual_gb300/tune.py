@@ -1,0 +1,152 @@
+"""Measures the fused path's launch choices and writes the AUTO table.
+
+    python -m tensor_allreduce_residual_gb300.tune sweep results.jsonl
+    python -m tensor_allreduce_residual_gb300.tune table results.jsonl
+
+`sweep` times every one-shot shape (units per thread x where the row is kept
+x when residual_out is written) and the two-shot path on the row shapes of
+the measured workloads, each shape in its own process (the shape override
+AR_ONESHOT_SHAPE is read once per process).  Calls are captured in a CUDA
+graph and replayed, so the numbers are device time without Python launch
+overhead.  `table` keeps the fastest choice per (element size, R, row
+length, tokens) and rewrites csrc/ar_auto_table.h.  This is the measured
+counterpart of heuristic_min_warp_number / selectImplementation.
+"""
+from __future__ import annotations
+
+import json
+import os
+import statistics
+import subprocess
+import sys
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+ROOT = os.path.dirname(PKG)
+TABLE = os.path.join(PKG, "csrc", "ar_auto_table.h")
+
+# (name, R, dtype, hidden, bias, token counts)
+CASES = [
+    ("tp_decode_R2_fp16_H4096", 2, "fp16", 4096, True, [1, 2, 4, 8, 16, 32, 64, 256, 1024, 8192]),
+    ("R8_bf16_H8192", 8, "bf16", 8192, False, [1, 8, 32, 64, 256, 512, 1024, 2048, 4096, 8192]),
+]
+SHAPES = ([f"{v}:{m}:{e}" for v in (1, 2, 4, 8) for m in (0, 1) for e in (0, 1)]
+          + [f"{v}:2:{e}" for v in (2, 4) for e in (0, 1)])
+
+
+def _graph_time(torch, fn, n=10, reps=5):
+    for _ in range(3):
+        fn()
+    torch.cuda.synchronize()
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        fn()
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            for _ in range(n):
+                fn()
+    ts = []
+    for _ in range(reps):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        g.replay()
+        b.record()
+        torch.cuda.synchronize()
+        ts.append(a.elapsed_time(b) / n)
+    return statistics.median(ts)
+
+
+def _measure(strategy: str, shape: str, out):
+    """Runs in a child process (AR_ONESHOT_SHAPE already set)."""
+    sys.path.insert(0, ROOT)
+    import torch
+
+    import tensor_allreduce_residual_gb300 as ar
+    import workloads
+    torch.cuda.set_device(0)
+    for name, R, dtype, H, has_bias, tokens in CASES:
+        for T in tokens:
+            f = workloads.fused_inputs(R, T, H, dtype, partial_dist=("N", 0.0, 1.0 / R),
+                                       residual_dist=("N", 0.0, 4.0),
+                                       bias_dist=("N", 0.0, 0.02) if has_bias else None,
+                                       weight_dist=("N", 1.0, 0.05), eps=1e-6, device="cuda")
+            o, r = torch.empty_like(f.residual), torch.empty_like(f.residual)
+            ws = torch.empty(ar.ar_workspace_size_rows(R, H, T, ar.dtype_code(f.residual.dtype)),
+                             dtype=torch.uint8, device="cuda")
+            fn = lambda: ar.ar_residual_rmsnorm(f.partials, f.residual, f.weight, f.eps, bias=f.bias,  # noqa: E731
+                                                out=o, residual_out=r, intermediate=ws, strategy=strategy)
+            try:
+                us = _graph_time(torch, fn) * 1e3
+            except ar.ARError:
+                continue
+            rec = {"case": name, "R": R, "esize": workloads.ELEM_SIZE[dtype], "units_row": H * workloads.ELEM_SIZE[dtype] // 16,
+                   "T": T, "strategy": strategy, "shape": shape, "us": round(us, 3)}
+            out.write(json.dumps(rec) + "\n")
+            out.flush()
+            del f, o, r, ws
+            torch.cuda.empty_cache()
+
+
+def sweep(path: str):
+    with open(path, "w") as out:
+        runs = [("TWOSHOT", "-")] + [("ONESHOT", s) for s in SHAPES]
+        for strategy, shape in runs:
+            env = dict(os.environ)
+            env.pop("AR_ONESHOT_SHAPE", None)
+            if shape != "-":
+                env["AR_ONESHOT_SHAPE"] = shape
+            res = subprocess.run([sys.executable, "-m", "tensor_allreduce_residual_gb300.tune", "_child",
+                                  strategy, shape], cwd=ROOT, env=env, capture_output=True, text=True)
+            if res.returncode != 0:
+                raise RuntimeError(f"sweep child {strategy} {shape} failed:\n{res.stderr[-2000:]}")
+            out.write(res.stdout)
+            out.flush()
+            print(f"swept {strategy} {shape}", file=sys.stderr)
+
+
+def table(path: str):
+    best = {}
+    with open(path) as f:
+        for line in f:
+            r = json.loads(line)
+            key = (r["esize"], r["R"], r["units_row"], r["T"])
+            if key not in best or r["us"] < best[key]["us"]:
+                best[key] = r
+    lines = []
+    groups = {}
+    for (esize, R, units, T), r in sorted(best.items()):
+        groups.setdefault((esize, R, units), []).append((T, r))
+    for (esize, R, units), items in groups.items():
+        items.sort()
+        for i, (T, r) in enumerate(items):
+            tmax = T if i + 1 < len(items) else 2147483647
+            if r["strategy"] == "TWOSHOT":
+                lines.append(f"    {{{esize}, {R}, {units}, {tmax}, 2, 0, 0, 0}},  // {r['case']} T={T}: "
+                             f"two-shot {r['us']} us")
+            else:
+                v, m, e = (int(x) for x in r["shape"].split(":"))
+                lines.append(f"    {{{esize}, {R}, {units}, {tmax}, 1, {v}, {m}, {e}}},  // {r['case']} T={T}: "
+                             f"one-shot {r['us']} us")
+    header = open(TABLE).read()
+    start = header.index("static const AutoEntry kAutoTable[] = {")
+    end = header.index("};", start)
+    body = "static const AutoEntry kAutoTable[] = {\n" + "\n".join(lines) + \
+        "\n    {0, 0, 0, 0, 0, 0, 0, 0},  // sentinel\n"
+    header = header[:start] + body + header[end:]
+    header = header.replace("// No measured entries yet: every shape takes the rule in ar_api.cu.\n", "")
+    with open(TABLE, "w") as f:
+        f.write(header)
+    print(f"wrote {len(lines)} entries to {TABLE}")
+
+
+if __name__ == "__main__":
+    cmd = sys.argv[1] if len(sys.argv) > 1 else ""
+    if cmd == "_child":
+        _measure(sys.argv[2], sys.argv[3], sys.stdout)
+    elif cmd == "sweep":
+        sweep(sys.argv[2])
+    elif cmd == "table":
+        table(sys.argv[2])
+    else:
+        print(__doc__)
+        sys.exit(2)

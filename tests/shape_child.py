@@ -1,0 +1,49 @@
+"""Child process for test_oneshot_shapes_gpu: parity of the one-shot fused path
+under the shape that AR_ONESHOT_SHAPE forces (set by the parent)."""
+import sys
+
+import torch
+
+import oracle
+import tensor_allreduce_residual_gb300 as ar
+import workloads
+from tests import tolerance as tol
+
+
+def check(inp, rows=None):
+    parts = [p.cuda() for p in inp.partials]
+    out, res = ar.ar_residual_rmsnorm(parts, inp.residual.cuda(), inp.weight.cuda(), inp.eps,
+                                      bias=None if inp.bias is None else inp.bias.cuda(), strategy="ONESHOT")
+    torch.cuda.synchronize()
+    if rows is not None:
+        idx = torch.tensor(rows)
+        inp = workloads.FusedInputs(inp.R, len(rows), inp.hidden, inp.dtype, inp.eps,
+                                    [p[idx].contiguous() for p in inp.partials], inp.residual[idx].contiguous(),
+                                    inp.weight, inp.bias)
+        out, res = out[idx.cuda()], res[idx.cuda()]
+    o_out, o_res, inv = oracle.residual_rmsnorm(inp.partials, inp.bias, inp.residual, inp.weight, inp.eps, inp.dtype)
+    T, H = inp.tokens, inp.hidden
+    terms = [p.reshape(T, H) for p in inp.partials]
+    if inp.bias is not None:
+        terms.append(inp.bias.expand(T, H).contiguous())
+    terms.append(inp.residual)
+    tol.check_sum(res.cpu(), o_res, terms, inp.dtype, "residual_out")
+    tol.check_fused_out(out.cpu(), o_out, terms, inp.weight, inv, inp.dtype, H, "out")
+
+
+def main():
+    torch.cuda.set_device(0)
+    check(workloads.tp_decode(5, seed=1))
+    check(workloads.decode_r8(3, seed=2))
+    check(workloads.fused_inputs(4, 33, 1024, "fp32", partial_dist=("N", 0.0, 0.25), residual_dist=("N", 0.0, 1.0),
+                                 bias_dist=("N", 0.0, 0.1), weight_dist=("N", 1.0, 0.1), eps=1e-5, seed=3))
+    check(workloads.fused_inputs(2, 9, 16384, "bf16", partial_dist=("N", 0.0, 0.5), residual_dist=("N", 0.0, 4.0),
+                                 bias_dist=None, weight_dist=("N", 1.0, 0.05), eps=1e-6, seed=4))
+    # more rows than resident blocks: persistent blocks stride over rows
+    big = workloads.tp_prefill(tokens=3000, seed=5)
+    check(big, rows=[0, 1, 151, 152, 999, 1500, 2047, 2048, 2998, 2999])
+    print("shape ok")
+
+
+if __name__ == "__main__":
+    sys.exit(main())

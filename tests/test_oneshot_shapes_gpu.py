@@ -1,0 +1,22 @@
+"""Every one-shot launch shape (registers / shared memory / persistent blocks,
+units per thread, residual_out written before or after the row barrier) gives
+oracle-parity results.  Each shape runs in a child process because the shape
+override is read once per process."""
+import os
+import subprocess
+import sys
+
+import pytest
+
+pytestmark = pytest.mark.gpu
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+SHAPES = ["1:0:1", "2:0:0", "4:0:1", "8:0:0", "1:1:0", "2:1:1", "4:1:0", "8:1:1", "2:2:1", "4:2:0", "4:2:1"]
+
+
+@pytest.mark.parametrize("shape", SHAPES)
+def test_oneshot_shape_parity(shape):
+    env = dict(os.environ, AR_ONESHOT_SHAPE=shape)
+    res = subprocess.run([sys.executable, "-m", "tests.shape_child"], cwd=ROOT, env=env,
+                         capture_output=True, text=True, timeout=600)
+    assert res.returncode == 0 and "shape ok" in res.stdout, res.stdout[-3000:] + res.stderr[-3000:]
