@@ -211,6 +211,48 @@ int ar_allreduce(const ar_params* p, int fusion_op, int strategy, ar_stream_t st
 int ar_query_strategy(int R, size_t n, int hidden, int dtype, int fusion_op,
                       int* chosen, int* warps_per_token);
 
+/* Size of the scratch array that ar_residual_rmsnorm_noalloc uses (1 MiB). */
+#define AR_NOALLOC_SCRATCH_BYTES ((size_t)1 << 20)
+
+/*
+ * ar_residual_rmsnorm_noalloc -- ar_residual_rmsnorm with strategy
+ * AR_TWOSHOT, except that the two-shot scratch (the per-chunk sums of
+ * squares) is not a caller buffer: it is an array of AR_NOALLOC_SCRATCH_BYTES
+ * that the library keeps in device memory.  The pages have no counterpart of
+ * this call.  It is for callers that cannot obtain device memory at the
+ * point of the call: code running under an allocator that owns all of the
+ * device's memory (a framework's caching pool, an inference engine that
+ * hands out memory only when it is built), or code that must not call
+ * cudaMalloc / cudaFree because they can wait on work already running on the
+ * device.  Inputs and outputs are still the caller's buffers, with the same
+ * meaning, layout, aliasing rules and results as in ar_residual_rmsnorm.
+ * The call allocates nothing: no cudaMalloc, no cudaFree, no allocating
+ * library routine.
+ *
+ * Limit: a call is accepted when ar_workspace_size_rows(R, hidden, tokens,
+ *   dtype) <= AR_NOALLOC_SCRATCH_BYTES (for example up to 16384 tokens of
+ *   hidden 8192, whatever the pointers' alignment).  Larger calls return
+ *   AR_ERR_WORKSPACE before anything is launched.
+ * Memory: every device that loads the library holds its own copy of the
+ *   array until the process exits.
+ * Set-up: the first call on a device, with that device current, looks up
+ *   the array's device address (cudaGetSymbolAddress) and keeps it for
+ *   later calls; make that first call before any stream capture begins.
+ *   A failed look-up returns AR_ERR_CUDA.
+ * Sharing: all calls on a device use the same array and it keeps what the
+ *   last call wrote.  Each call writes every entry it reads before reading
+ *   it, so nothing is cleared between calls.  Calls whose work overlaps on
+ *   the GPU (different streams not ordered by events, or several host
+ *   threads) race on the array and may return wrong results: order them.
+ * Errors: those of ar_residual_rmsnorm with AR_TWOSHOT, plus AR_ERR_WORKSPACE
+ *   for a call beyond the limit and AR_ERR_UNSUPPORTED for a device index
+ *   of 64 or more.
+ */
+int ar_residual_rmsnorm_noalloc(const void* const* partials, int R, const void* bias,
+                                const void* residual, const void* weight, float eps,
+                                int hidden, int tokens, void* out, void* residual_out,
+                                int dtype, ar_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

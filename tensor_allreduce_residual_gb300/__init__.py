@@ -29,6 +29,7 @@ AR_FUSION_NONE, AR_FUSION_RESIDUAL_RMS_NORM = 0, 1
 # status codes
 AR_OK, AR_ERR_INVALID_ARG, AR_ERR_UNSUPPORTED, AR_ERR_WORKSPACE, AR_ERR_CUDA = 0, -1, -2, -3, -4
 AR_MAX_RANKS = 16
+AR_NOALLOC_SCRATCH_BYTES = 1 << 20
 
 STRATEGIES = {"NCCL": AR_NCCL, "ONESHOT": AR_ONESHOT, "TWOSHOT": AR_TWOSHOT, "AUTO": AR_AUTO}
 STRATEGY_NAMES = {v: k for k, v in STRATEGIES.items()}
@@ -85,6 +86,8 @@ def lib() -> ctypes.CDLL:
     L.ar_allreduce.argtypes, L.ar_allreduce.restype = [ctypes.POINTER(ArParams), i, i, vp], i
     L.ar_query_strategy.argtypes = [i, sz, i, i, i, ctypes.POINTER(i), ctypes.POINTER(i)]
     L.ar_query_strategy.restype = i
+    L.ar_residual_rmsnorm_noalloc.argtypes = [pvp, i, vp, vp, vp, ctypes.c_float, i, i, vp, vp, i, vp]
+    L.ar_residual_rmsnorm_noalloc.restype = i
     _lib = L
     return L
 
@@ -215,6 +218,32 @@ def ar_residual_rmsnorm(partials: Sequence[torch.Tensor], residual: torch.Tensor
         _dev_ptr(weight, "weight"), ctypes.c_float(eps), hidden, tokens, _dev_ptr(out, "out"),
         _dev_ptr(residual_out, "residual_out"), ws_ptr, ws_bytes, code, st, _stream_handle(stream))
     _check("ar_residual_rmsnorm", status)
+    return out, residual_out
+
+
+def ar_residual_rmsnorm_noalloc(partials: Sequence[torch.Tensor], residual: torch.Tensor, weight: torch.Tensor,
+                                eps: float, bias: Optional[torch.Tensor] = None,
+                                out: torch.Tensor = None, residual_out: torch.Tensor = None, stream=None):
+    """(out, residual_out) of the two-shot fused call whose scratch is the library's own array.
+
+    For callers that must not allocate device memory during the call: ``out``
+    and ``residual_out`` are required (this wrapper creates no tensor either).
+    Accepts shapes with ar_workspace_size_rows(...) <= AR_NOALLOC_SCRATCH_BYTES.
+    """
+    if residual.dim() != 2:
+        raise ValueError("residual must be [tokens, hidden]")
+    if out is None or residual_out is None:
+        raise ValueError("out and residual_out must be given: this call allocates nothing")
+    tokens, hidden = residual.shape
+    for k, p in enumerate(partials):
+        if p.numel() != residual.numel() or p.dtype != residual.dtype:
+            raise ValueError(f"partials[{k}] must match residual in size and dtype")
+    ptrs = _ptr_array([_dev_ptr(p, f"partials[{k}]") for k, p in enumerate(partials)])
+    status = lib().ar_residual_rmsnorm_noalloc(
+        ptrs, len(partials), _dev_ptr(bias, "bias"), _dev_ptr(residual, "residual"),
+        _dev_ptr(weight, "weight"), ctypes.c_float(eps), hidden, tokens, _dev_ptr(out, "out"),
+        _dev_ptr(residual_out, "residual_out"), dtype_code(residual.dtype), _stream_handle(stream))
+    _check("ar_residual_rmsnorm_noalloc", status)
     return out, residual_out
 
 
