@@ -38,7 +38,7 @@ R, TOKENS, HIDDEN, EPS = 8, 8192, 8192, 1e-6
 DATA = ("synthetic, seeded: partials N(0,1/8), residual N(0,4), bias N(0,0.02), weight N(1,0.05) "
         "(second argument = variance), drawn in fp32 and rounded to bf16")
 FALLBACK_HBM_GBS = 6800.0
-KERNEL_SOURCES = ["ar_kernels.cuh", "ar_launch.cuh", "ar_internal.h", "ar_api.cu"]
+KERNEL_SOURCES = ["ar_kernels.cuh", "ar_tma.cuh", "ar_launch.cuh", "ar_internal.h", "ar_api.cu", "ar_auto_table.h"]
 
 
 def parse_args():
@@ -173,7 +173,7 @@ def run_ours(args, rank, world, local_rank):
 
     import tensor_allreduce_residual_gb300 as ar
     import workloads
-    from tensor_allreduce_residual_gb300.dist import max_over_ranks
+    from tensor_allreduce_residual_gb300.dist import max_over_ranks, shard_range
 
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
@@ -184,7 +184,10 @@ def run_ours(args, rank, world, local_rank):
             dist.barrier()
         torch.cuda.synchronize()
 
-    # Inputs: this rank's block of rows, drawn on the GPU (seeded per rank).
+    # Inputs: this rank's block of the global batch's rows (TOKENS per GPU),
+    # drawn on the GPU, seeded per rank.
+    row_begin, row_end = shard_range(TOKENS * world, rank, world)
+    assert row_end - row_begin == TOKENS
     inp = workloads.tp_prefill(TOKENS, HIDDEN, seed=rank, device="cuda")
     parts, resid, weight, bias = inp.partials, inp.residual, inp.weight, inp.bias
     out = torch.empty_like(resid)
@@ -192,8 +195,9 @@ def run_ours(args, rank, world, local_rank):
     ws = torch.empty(ar.ar_workspace_size_rows(R, HIDDEN, TOKENS, ar.AR_BF16), dtype=torch.uint8, device=dev)
     bytes_call = algorithmic_bytes(R, TOKENS, HIDDEN, 2)
     stream = torch.cuda.current_stream()
-    chosen, warps = ar.ar_query_strategy(R, TOKENS * HIDDEN, HIDDEN, ar.AR_BF16)
-    resolved = ar.STRATEGY_NAMES[chosen] if args.strategy == "AUTO" else args.strategy
+    plan = ar.ar_query_launch(R, HIDDEN, TOKENS, ar.AR_BF16, args.strategy)
+    resolved = ar.STRATEGY_NAMES[plan["strategy"]]
+    warps = (plan["threads_per_row"] + 31) // 32
     launches_per_step = 1 if resolved == "ONESHOT" else 2
 
     def step(strategy=args.strategy):
@@ -233,7 +237,7 @@ def run_ours(args, rank, world, local_rank):
     peak, peak_src = measured_peaks()
     mean_launch_ms = statistics.fmean(per_step)
     achieved = bytes_call / (mean_launch_ms * 1e-3) / 1e9
-    kernel_tag = "k_fused_oneshot" if resolved == "ONESHOT" else "k_twoshot_phase1+phase2"
+    kernel_tag = plan["kernel_name"]
     traffic = profiled_traffic(kernel_tag)
     roofline = {"bound": "hbm", "kernel": kernel_tag, "achieved": round(achieved, 1), "peak": peak,
                 "unit": "GB/s", "frac": round(achieved / peak, 4), "peak_source": peak_src,
@@ -284,6 +288,7 @@ def run_ours(args, rank, world, local_rank):
         "config": {"workload": WORKLOAD.replace("tokens=8192", f"tokens={TOKENS}"), "R": R, "tokens_per_gpu": TOKENS, "global_tokens": TOKENS * world,
                    "hidden": HIDDEN, "io_dtype": "bf16", "eps": EPS, "strategy": args.strategy,
                    "resolved_strategy": resolved, "warps_per_token": warps,
+                   "launch": {k: v for k, v in plan.items() if k != "strategy"},
                    "bytes_per_call": bytes_call, "parallelism": f"rows sharded over {world} GPU(s), no collective",
                    "l2": f"inputs larger than L2 ({bytes_call / 1e9:.2f} GB per call vs 129 MB L2): no flush between steps"},
         "us_per_call": round(ms_step * 1e3, 2), "frac_of_peak": round(value / world / peak, 4),
@@ -321,13 +326,45 @@ def _time_cold(torch, fn, stream, flush, n):
     return statistics.median(ts)
 
 
+def _time_graph(torch, fn, n=20, reps=5):
+    """Median device time per call of `fn`, captured n times in a CUDA graph and replayed (no host overhead)."""
+    for _ in range(3):
+        fn()
+    torch.cuda.synchronize()
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        fn()
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            for _ in range(n):
+                fn()
+    ts = []
+    for _ in range(reps):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        g.replay()
+        b.record()
+        torch.cuda.synchronize()
+        ts.append(a.elapsed_time(b) / n)
+    del g
+    return statistics.median(ts)
+
+
 def run_extras(ar, torch, workloads, parts, resid, weight, bias, out, res_out, ws, bytes_call, stream):
-    """Secondary numbers: each fixed strategy on the prefill inputs, decode latency, reduce-only bandwidth."""
+    """Secondary numbers: each fixed strategy on the prefill inputs, decode latency, reduce-only bandwidth.
+
+    Calls run on the current stream (the capturing stream inside a graph capture).
+
+    us_warm / us_cold: one Python call per timed call (host launch overhead
+    included; cold = L2 flushed before each call).  us_graph: device time per
+    call from a replayed CUDA graph of 20 calls (L2 warm).
+    """
     ex = {}
     for s in ("ONESHOT", "TWOSHOT"):
         ms = _time_calls(torch, lambda s=s: ar.ar_residual_rmsnorm(
             parts, resid, weight, EPS, bias=bias, out=out, residual_out=res_out, intermediate=ws,
-            strategy=s, stream=stream), stream, 100)
+            strategy=s), stream, 100)
         ex[f"prefill_{s}"] = {"us_per_call": round(ms * 1e3, 2), "GBps": round(bytes_call / ms / 1e6, 1)}
     flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
     dec = {}
@@ -335,9 +372,10 @@ def run_extras(ar, torch, workloads, parts, resid, weight, bias, out, res_out, w
         f = workloads.tp_decode(T, device="cuda")
         o, r = torch.empty_like(f.residual), torch.empty_like(f.residual)
         fn = lambda f=f, o=o, r=r: ar.ar_residual_rmsnorm(f.partials, f.residual, f.weight, f.eps, bias=f.bias,  # noqa: E731
-                                                          out=o, residual_out=r, strategy="ONESHOT", stream=stream)
+                                                          out=o, residual_out=r, strategy="ONESHOT")
         dec[f"T{T}"] = {"us_warm": round(_time_calls(torch, fn, stream, 200) * 1e3, 2),
-                        "us_cold": round(_time_cold(torch, fn, stream, flush, 30) * 1e3, 2)}
+                        "us_cold": round(_time_cold(torch, fn, stream, flush, 30) * 1e3, 2),
+                        "us_graph": round(_time_graph(torch, fn) * 1e3, 2)}
     ex["tp_decode_R2_fp16_H4096"] = dec
     r8 = {}
     for T in workloads.DECODE_R8_TOKENS:
@@ -346,24 +384,31 @@ def run_extras(ar, torch, workloads, parts, resid, weight, bias, out, res_out, w
         w8 = torch.empty(ar.ar_workspace_size_rows(8, 8192, T, ar.AR_BF16), dtype=torch.uint8, device="cuda")
         fn = lambda f=f, o=o, r=r, w8=w8: ar.ar_residual_rmsnorm(f.partials, f.residual, f.weight, f.eps,  # noqa: E731
                                                                  out=o, residual_out=r, intermediate=w8,
-                                                                 strategy="AUTO", stream=stream)
+                                                                 strategy="AUTO")
         b = algorithmic_bytes(8, T, 8192, 2, has_bias=False)
         cold = _time_cold(torch, fn, stream, flush, 30)
         r8[f"T{T}"] = {"us_warm": round(_time_calls(torch, fn, stream, 100) * 1e3, 2), "us_cold": round(cold * 1e3, 2),
-                       "GBps_cold": round(b / cold / 1e6, 1),
+                       "GBps_cold": round(b / cold / 1e6, 1), "us_graph": round(_time_graph(torch, fn) * 1e3, 2),
                        "auto": ar.STRATEGY_NAMES[ar.ar_query_strategy(8, T * 8192, 8192, ar.AR_BF16)[0]]}
     ex["decode_R8_bf16_H8192"] = r8
     del flush
+    # Reduce-only sweep, R=4 fp16, n = 2^9 .. 2^27: device time per call
+    # (graph replay).  Working sets below L2 (129 MB) are partly served by L2.
     red = {}
-    n = 1 << 27
-    s_in = workloads.reduce_only(n, device="cuda")
-    o = torch.empty_like(s_in.partials[0])
-    b = workloads.sum_algorithmic_bytes(4, n, "fp16")
-    for s in ("ONESHOT", "TWOSHOT"):
-        ms = _time_calls(torch, lambda s=s: ar.ar_sum(s_in.partials, out=o, strategy=s, stream=stream), stream, 20)
-        red[s] = {"us_per_call": round(ms * 1e3, 1), "GBps": round(b / ms / 1e6, 1)}
-    ex["reduce_only_R4_fp16_n2^27"] = red
-    del s_in, o
+    big = workloads.reduce_only(1 << 27, device="cuda")
+    o_big = torch.empty_like(big.partials[0])
+    for k in range(9, 28):
+        n = 1 << k
+        parts_n = [p[:n] for p in big.partials]
+        o = o_big[:n]
+        b = workloads.sum_algorithmic_bytes(4, n, "fp16")
+        row = {}
+        for s in ("ONESHOT", "TWOSHOT", "AUTO"):
+            ms = _time_graph(torch, lambda s=s: ar.ar_sum(parts_n, out=o, strategy=s), n=10, reps=3)
+            row[s] = {"us": round(ms * 1e3, 2), "GBps": round(b / ms / 1e6, 1)}
+        red[f"2^{k}"] = row
+    ex["reduce_only_R4_fp16_sweep"] = red
+    del big, o_big
     torch.cuda.empty_cache()
     return ex
 

@@ -20,8 +20,9 @@
  *   - Memory: every buffer is owned by the caller and lives in device
  *     memory of the current device.  The `partials` array itself is a HOST
  *     array of R device pointers; it is read during the call only.  The
- *     library allocates nothing and keeps no mutable state; calls are
- *     thread-safe.
+ *     library allocates nothing.  Its only device state is the scratch
+ *     array of ar_residual_rmsnorm_noalloc and a count of bounded waits
+ *     that gave up (ar_device_status); every other call is thread-safe.
  *   - Layout: tensors are dense and row-major.  The fused call sees
  *     [tokens, hidden] rows; bias and weight are [hidden]; every tensor of
  *     one call has the same element type (ar_dtype); eps is a float.
@@ -66,7 +67,8 @@ enum {
     AR_ERR_INVALID_ARG = -1,  /* bad R, NULL required pointer, bad size, eps < 0 ... */
     AR_ERR_UNSUPPORTED = -2,  /* NCCL strategy, unknown dtype/strategy/fusion, row too long for ONESHOT */
     AR_ERR_WORKSPACE = -3,    /* TWOSHOT fused without a large enough workspace */
-    AR_ERR_CUDA = -4          /* the CUDA runtime reported an error at launch */
+    AR_ERR_CUDA = -4,         /* the CUDA runtime reported an error at launch */
+    AR_ERR_TIMEOUT = -5       /* a kernel gave up a bounded wait (see ar_device_status) */
 };
 
 /* MAX_RANKS_PER_NODE ("type.d2", AllReduceParams::peer_comm_buffer_ptrs):
@@ -210,6 +212,56 @@ int ar_allreduce(const ar_params* p, int fusion_op, int strategy, ar_stream_t st
  */
 int ar_query_strategy(int R, size_t n, int hidden, int dtype, int fusion_op,
                       int* chosen, int* warps_per_token);
+
+/* Kernels a fused call can run (ar_launch_plan::kernel). */
+typedef enum {
+    AR_KERNEL_ONESHOT_REGISTERS = 1,  /* k_fused_oneshot, row sums in registers */
+    AR_KERNEL_ONESHOT_SHARED = 2,     /* k_fused_oneshot, row sums in shared memory */
+    AR_KERNEL_ONESHOT_PERSISTENT = 3, /* k_fused_oneshot_persist */
+    AR_KERNEL_ONESHOT_BULK = 4,       /* k_fused_oneshot_tma: persistent, fed by bulk copies */
+    AR_KERNEL_TWOSHOT = 5             /* k_twoshot_phase1 then k_twoshot_phase2 */
+} ar_kernel;
+
+/* Launch plan of a fused call (see ar_query_launch). */
+typedef struct {
+    int strategy;          /* AR_ONESHOT or AR_TWOSHOT */
+    int kernel;            /* ar_kernel */
+    int threads_per_row;   /* threads that cooperate on one row */
+    int units_per_thread;  /* one-shot: 16-byte vectors (or elements) per thread per row;
+                              bulk-copy kernel: chunks per row */
+    int rows_per_block;    /* rows a block holds at once */
+    int threads_per_block;
+    int blocks_per_sm;     /* persistent kernels: blocks per SM the grid is sized for; else 0 */
+    int stages;            /* bulk-copy kernel: ring slots per block; else 0 */
+    int smem_bytes;        /* dynamic shared memory per block */
+    int early_residual;    /* one-shot: residual_out written before the row's norm is known */
+} ar_launch_plan;
+
+/*
+ * ar_query_launch -- the kernel and launch shape that ar_residual_rmsnorm
+ * would use for this shape and strategy, assuming 16-byte aligned pointers
+ * and a large enough workspace (the kernelLaunchConfig /
+ * heuristic_min_warp_number analogue, "allreduce.d2").  Launches nothing.
+ * Errors: AR_ERR_INVALID_ARG (bad R, hidden, tokens or NULL plan),
+ *         AR_ERR_UNSUPPORTED (unknown dtype or strategy, AR_NCCL, or
+ *         AR_ONESHOT for a row too long for the one-shot kernels).
+ */
+int ar_query_launch(int R, int hidden, int tokens, int dtype, int strategy, ar_launch_plan* plan);
+
+/*
+ * ar_device_status -- whether any kernel of this library on the current
+ * device gave up a bounded wait since the last call.  The one-shot fused
+ * kernel that streams rows through a shared-memory ring waits on barriers
+ * that its own copies complete; each such wait is limited to one second,
+ * after which the kernel stops early (its outputs are then incomplete),
+ * records the event and returns instead of hanging.  No pages' counterpart:
+ * the pages' kernels wait on peer GPUs through block_barrier /
+ * multi_gpu_barrier ("allreduce.d2"), which have no equivalent here.
+ * Returns AR_OK (nothing recorded), AR_ERR_TIMEOUT (something was recorded;
+ * the record is cleared), or AR_ERR_CUDA.  Synchronous: it reads device
+ * memory, so it waits for work queued on the legacy default stream.
+ */
+int ar_device_status(void);
 
 /* Size of the scratch array that ar_residual_rmsnorm_noalloc uses (1 MiB). */
 #define AR_NOALLOC_SCRATCH_BYTES ((size_t)1 << 20)

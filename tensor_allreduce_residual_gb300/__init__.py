@@ -27,7 +27,7 @@ AR_NCCL, AR_ONESHOT, AR_TWOSHOT, AR_AUTO = 0, 1, 2, 3
 # ar_fusion_op (AllReduceFusionOp values)
 AR_FUSION_NONE, AR_FUSION_RESIDUAL_RMS_NORM = 0, 1
 # status codes
-AR_OK, AR_ERR_INVALID_ARG, AR_ERR_UNSUPPORTED, AR_ERR_WORKSPACE, AR_ERR_CUDA = 0, -1, -2, -3, -4
+AR_OK, AR_ERR_INVALID_ARG, AR_ERR_UNSUPPORTED, AR_ERR_WORKSPACE, AR_ERR_CUDA, AR_ERR_TIMEOUT = 0, -1, -2, -3, -4, -5
 AR_MAX_RANKS = 16
 AR_NOALLOC_SCRATCH_BYTES = 1 << 20
 
@@ -63,6 +63,17 @@ class ArParams(ctypes.Structure):
     ]
 
 
+class ArLaunchPlan(ctypes.Structure):
+    """Mirror of the C struct ar_launch_plan."""
+    _fields_ = [(name, ctypes.c_int) for name in (
+        "strategy", "kernel", "threads_per_row", "units_per_thread", "rows_per_block", "threads_per_block",
+        "blocks_per_sm", "stages", "smem_bytes", "early_residual")]
+
+
+# ar_kernel codes and the kernel names they stand for
+KERNEL_NAMES = {1: "k_fused_oneshot", 2: "k_fused_oneshot", 3: "k_fused_oneshot_persist",
+                4: "k_fused_oneshot_tma", 5: "k_twoshot_phase1+k_twoshot_phase2"}
+
 _lib: Optional[ctypes.CDLL] = None
 
 
@@ -88,6 +99,9 @@ def lib() -> ctypes.CDLL:
     L.ar_query_strategy.restype = i
     L.ar_residual_rmsnorm_noalloc.argtypes = [pvp, i, vp, vp, vp, ctypes.c_float, i, i, vp, vp, i, vp]
     L.ar_residual_rmsnorm_noalloc.restype = i
+    L.ar_device_status.argtypes, L.ar_device_status.restype = [], i
+    L.ar_query_launch.argtypes = [i, i, i, i, i, ctypes.POINTER(ArLaunchPlan)]
+    L.ar_query_launch.restype = i
     _lib = L
     return L
 
@@ -145,6 +159,11 @@ def ar_strerror(code: int) -> str:
     return lib().ar_strerror(code).decode()
 
 
+def ar_device_status() -> int:
+    """AR_OK, or AR_ERR_TIMEOUT if a kernel gave up a bounded wait since the last call (synchronous)."""
+    return lib().ar_device_status()
+
+
 def ar_workspace_size(R: int, n: int, dtype) -> int:
     code = dtype if isinstance(dtype, int) else dtype_code(dtype)
     return int(lib().ar_workspace_size(R, n, code))
@@ -162,6 +181,16 @@ def ar_query_strategy(R: int, n: int, hidden: int, dtype, fusion_op: int = AR_FU
     _check("ar_query_strategy",
            lib().ar_query_strategy(R, n, hidden, code, fusion_op, ctypes.byref(chosen), ctypes.byref(warps)))
     return chosen.value, warps.value
+
+
+def ar_query_launch(R: int, hidden: int, tokens: int, dtype, strategy="AUTO") -> dict:
+    """The kernel and launch shape ar_residual_rmsnorm would use (aligned pointers, workspace given)."""
+    code = dtype if isinstance(dtype, int) else dtype_code(dtype)
+    plan = ArLaunchPlan()
+    _check("ar_query_launch", lib().ar_query_launch(R, hidden, tokens, code, _strategy(strategy), ctypes.byref(plan)))
+    d = {name: getattr(plan, name) for name, _ in ArLaunchPlan._fields_}
+    d["kernel_name"] = KERNEL_NAMES.get(plan.kernel, "?")
+    return d
 
 
 def ar_sum(partials: Sequence[torch.Tensor], out: Optional[torch.Tensor] = None,

@@ -69,8 +69,39 @@ int next_pow2(int v)
 // at least 128 threads.  Register-resident rows are limited by the registers
 // a thread may use, staged rows by shared memory.  Returns false when the
 // row does not fit (then only the two-shot path can take it).
-bool oneshot_shape(int units_row, int vpt, int lanes, bool packed, int mode, int R, OneShotShape* sh)
+// Bulk-copy-fed persistent shape (mode kTma): vpt = chunks per row, one
+// consumer thread per vector of a chunk (a multiple of 32), and as many ring
+// slots as the shared memory of `blocks_per_sm` blocks per SM allows.
+bool tma_shape(int units_row, int vpt, int R, int blocks_per_sm, OneShotShape* sh)
 {
+    if (!(vpt == 1 || vpt == 2 || vpt == 4 || vpt == 8) || blocks_per_sm < 1 || blocks_per_sm > 4)
+        return false;
+    const int nc = ((units_row + vpt - 1) / vpt + 31) / 32 * 32;
+    if (nc > ar::tma_max_consumers(vpt) || (units_row + nc - 1) / nc > vpt)
+        return false;
+    int budget = ar::kSmemPerSM / blocks_per_sm - ar::kSmemReservedPerBlock;
+    if (budget > ar::kSmemPerBlockMax)
+        budget = ar::kSmemPerBlockMax;
+    int stages = ar::kTmaMaxStages;
+    while (stages >= ar::kTmaMinStages && ar::tma_smem_bytes(R, nc, stages) > static_cast<size_t>(budget))
+        --stages;
+    if (stages < ar::kTmaMinStages)
+        return false;
+    sh->tpr = nc;
+    sh->vpt = vpt;
+    sh->rows = 1;
+    sh->mode = ar::kTma;
+    sh->smem_bytes = static_cast<int>(ar::tma_smem_bytes(R, nc, stages));
+    sh->stages = stages;
+    sh->blocks_per_sm = blocks_per_sm;
+    return true;
+}
+
+bool oneshot_shape(int units_row, int vpt, int lanes, bool packed, int mode, int R, OneShotShape* sh,
+                   int blocks_per_sm = 1)
+{
+    if (mode == ar::kTma)
+        return packed && tma_shape(units_row, vpt, R, blocks_per_sm, sh);
     const int max_vpt = packed ? ar::kMaxVPTVec : ar::kMaxVPTScalar;
     const bool stage = mode != ar::kRegisters;
     if (vpt < 1 || vpt > max_vpt || (stage && (!packed || vpt > ar::kMaxVPTVec)))
@@ -124,14 +155,15 @@ const ar::AutoEntry* table_lookup(int esize, int R, int units_row, int tokens)
     return nullptr;
 }
 
-// Measurement override of the one-shot shape: AR_ONESHOT_SHAPE="vpt:mode" or
-// "vpt:mode:early" (e.g. "4:1" or "2:0:1") replaces the table and the rule
-// for every packed call.  Read once per process; used to sweep shapes when
-// building the AUTO table.
+// Measurement override of the one-shot shape: AR_ONESHOT_SHAPE="vpt:mode",
+// "vpt:mode:early" or "vpt:mode:early:blocks_per_sm" (e.g. "4:1", "2:0:1",
+// "4:3:0:2") replaces the table and the rule for every packed call.  Read
+// once per process; used to sweep shapes when building the AUTO table.
 struct ShapeOverride {
     int vpt = 0;
     int mode = 0;
     int early = 0;
+    int blocks_per_sm = 1;
 };
 
 const ShapeOverride& shape_override()
@@ -139,12 +171,13 @@ const ShapeOverride& shape_override()
     static const ShapeOverride ov = [] {
         ShapeOverride o;
         if (const char* env = std::getenv("AR_ONESHOT_SHAPE")) {
-            int v = 0, st = 0, early = 0;
-            const int got = std::sscanf(env, "%d:%d:%d", &v, &st, &early);
-            if (got >= 2 && v > 0 && st >= 0 && st <= 2) {
+            int v = 0, st = 0, early = 0, bps = 1;
+            const int got = std::sscanf(env, "%d:%d:%d:%d", &v, &st, &early, &bps);
+            if (got >= 2 && v > 0 && st >= 0 && st <= ar::kTma) {
                 o.vpt = v;
                 o.mode = st;
-                o.early = got == 3 && early != 0;
+                o.early = got >= 3 && early != 0;
+                o.blocks_per_sm = got == 4 && bps > 0 ? bps : 1;
             }
         }
         return o;
@@ -167,6 +200,7 @@ FusedPlan plan_fused(int esize, int R, int hidden, int tokens, bool packed, int 
     int vpt = rule_vpt(units_row, tokens, lanes, packed);
     int mode = ar::kRegisters;
     int early = 1;
+    int bps = 1;
     int auto_strategy = AR_ONESHOT;
     if (packed) {
         if (const ar::AutoEntry* e = table_lookup(esize, R, units_row, tokens)) {
@@ -175,6 +209,7 @@ FusedPlan plan_fused(int esize, int R, int hidden, int tokens, bool packed, int 
                 vpt = e->vpt;
                 mode = e->mode;
                 early = e->early;
+                bps = e->blocks_per_sm > 0 ? e->blocks_per_sm : 1;
             }
         }
         const ShapeOverride& ov = shape_override();
@@ -182,9 +217,10 @@ FusedPlan plan_fused(int esize, int R, int hidden, int tokens, bool packed, int 
             vpt = ov.vpt;
             mode = ov.mode;
             early = ov.early;
+            bps = ov.blocks_per_sm;
         }
     }
-    p.oneshot_ok = oneshot_shape(units_row, vpt, lanes, packed, mode, R, &p.shape);
+    p.oneshot_ok = oneshot_shape(units_row, vpt, lanes, packed, mode, R, &p.shape, bps);
     if (!p.oneshot_ok)  // the chosen shape does not fit this row: the rule's shape
         p.oneshot_ok = oneshot_shape(units_row, rule_vpt(units_row, tokens, lanes, packed), lanes,
                                      packed, ar::kRegisters, R, &p.shape);
@@ -218,6 +254,7 @@ const char* ar_strerror(int code)
     case AR_ERR_UNSUPPORTED: return "unsupported configuration";
     case AR_ERR_WORKSPACE: return "workspace missing or too small";
     case AR_ERR_CUDA: return "CUDA launch error";
+    case AR_ERR_TIMEOUT: return "a kernel gave up a bounded wait";
     default: return "unknown status code";
     }
 }
@@ -373,6 +410,80 @@ int ar_allreduce(const ar_params* p, int fusion_op, int strategy, ar_stream_t st
     return ar_residual_rmsnorm(p->partials, p->R, p->bias, p->residual, p->weight, p->eps,
                                p->hidden, tokens, p->out, p->residual_out, p->workspace,
                                p->workspace_bytes, p->dtype, strategy, stream);
+}
+
+int ar_query_launch(int R, int hidden, int tokens, int dtype, int strategy, ar_launch_plan* plan)
+{
+    if (R < 1 || R > AR_MAX_RANKS || hidden < 1 || tokens < 0 || plan == nullptr)
+        return AR_ERR_INVALID_ARG;
+    const int esize = esize_of(dtype);
+    if (esize == 0)
+        return AR_ERR_UNSUPPORTED;
+    if (int st = strategy_status(strategy))
+        return st;
+    const int lanes = 16 / esize;
+    const bool packed = hidden % lanes == 0;
+    const FusedPlan fp = plan_fused(esize, R, hidden, tokens, packed, strategy);
+    if (fp.strategy == AR_ONESHOT && !fp.oneshot_ok)
+        return AR_ERR_UNSUPPORTED;
+    ar_launch_plan p{};
+    p.strategy = fp.strategy;
+    if (fp.strategy == AR_TWOSHOT) {
+        p.kernel = AR_KERNEL_TWOSHOT;
+        p.threads_per_row = ar::kFlatThreads * twoshot_nchunk(packed ? hidden / lanes : hidden);
+        p.units_per_thread = ar::kChunkVPT;
+        p.rows_per_block = 1;
+        p.threads_per_block = ar::kFlatThreads;
+    } else {
+        const OneShotShape& sh = fp.shape;
+        p.threads_per_row = sh.tpr;
+        p.units_per_thread = sh.vpt;
+        p.rows_per_block = sh.rows;
+        p.early_residual = sh.early_residual;
+        p.smem_bytes = sh.mode == ar::kRegisters ? 0 : sh.smem_bytes;
+        switch (sh.mode) {
+        case ar::kRegisters:
+            p.kernel = AR_KERNEL_ONESHOT_REGISTERS;
+            p.threads_per_block = sh.tpr * sh.rows;
+            break;
+        case ar::kStaged:
+            p.kernel = AR_KERNEL_ONESHOT_SHARED;
+            p.threads_per_block = sh.tpr * sh.rows;
+            break;
+        case ar::kPersistent:
+            p.kernel = AR_KERNEL_ONESHOT_PERSISTENT;
+            p.threads_per_block = sh.tpr;
+            break;
+        default:
+            p.kernel = AR_KERNEL_ONESHOT_BULK;
+            p.threads_per_block = sh.tpr + 32;
+            p.blocks_per_sm = sh.blocks_per_sm;
+            p.stages = sh.stages;
+            break;
+        }
+    }
+    *plan = p;
+    return AR_OK;
+}
+
+int ar_device_status(void)
+{
+    unsigned int total = 0;
+    cudaError_t e = cudaSuccess;
+    const int dtypes[] = {AR_FP32, AR_FP16, AR_BF16};
+    for (int dt : dtypes) {
+        unsigned int n = 0;
+        const cudaError_t ed = by_dtype(dt, [&](auto tag) {
+            using T = decltype(tag);
+            return ar::take_wait_timeouts<T>(&n);
+        });
+        if (ed != cudaSuccess)
+            e = ed;
+        total += n;
+    }
+    if (e != cudaSuccess)
+        return AR_ERR_CUDA;
+    return total != 0 ? AR_ERR_TIMEOUT : AR_OK;
 }
 
 int ar_query_strategy(int R, size_t n, int hidden, int dtype, int fusion_op, int* chosen,

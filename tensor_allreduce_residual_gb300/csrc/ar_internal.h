@@ -70,7 +70,8 @@ struct FusedArgs {
 enum OneShotMode {
     kRegisters = 0,   // registers, one block per `rows` rows
     kStaged = 1,      // shared memory, one block per `rows` rows
-    kPersistent = 2   // shared memory, persistent blocks striding over rows
+    kPersistent = 2,  // shared memory, persistent blocks striding over rows
+    kTma = 3          // registers, persistent blocks fed by bulk copies into a shared-memory ring
 };
 
 // One-shot fused launch shape: `tpr` threads per row (a power of two),
@@ -83,6 +84,8 @@ struct OneShotShape {
     int mode;
     int smem_bytes;
     int early_residual;  // write residual_out before the row barrier
+    int stages;          // kTma: ring slots per block
+    int blocks_per_sm;   // kTma: resident blocks per SM
 };
 
 // Largest block of the persistent one-shot kernel (it keeps the next row's
@@ -91,6 +94,28 @@ constexpr int kMaxPersistThreads = 512;
 
 // Largest dynamic shared memory a staged one-shot block may use.
 constexpr int kMaxStageBytes = 96 * 1024;
+
+// One-shot fused path fed by bulk copies (mode kTma): consumer threads per
+// block for `cpr` chunks per row (each keeps cpr * lanes fp32 values of its
+// row in registers, so longer rows per thread allow fewer threads), the ring
+// depth limits, and the shared memory one block may use.
+__host__ __device__ constexpr int tma_max_consumers(int cpr)
+{
+    return cpr <= 2 ? 512 : (cpr == 4 ? 256 : 128);
+}
+constexpr int kTmaMinStages = 2;
+constexpr int kTmaMaxStages = 16;
+constexpr int kSmemPerBlockMax = 227 * 1024;  // opt-in dynamic shared memory of one block
+constexpr int kSmemPerSM = 228 * 1024;        // shared memory of one SM
+constexpr int kSmemReservedPerBlock = 1024;   // taken by the runtime from each resident block
+
+// Shared memory of one kTma block: `stages` ring slots of (R + 1) * nc
+// 16-byte vectors, then a full and an empty barrier per slot (8 bytes each),
+// then the row-reduction scratch, [2][32] floats.
+__host__ __device__ constexpr size_t tma_smem_bytes(int R, int nc, int stages)
+{
+    return static_cast<size_t>(stages) * (R + 1) * nc * 16 + static_cast<size_t>(stages) * 16 + 2 * 32 * 4;
+}
 
 // Launchers, explicitly instantiated for float, __half and __nv_bfloat16 in
 // the per-dtype translation units.  Each returns the cudaError_t of the launch.
@@ -102,5 +127,10 @@ cudaError_t launch_fused_oneshot(const FusedArgs& a, bool packed, OneShotShape s
 
 template <typename T>
 cudaError_t launch_fused_twoshot(const FusedArgs& a, bool packed, cudaStream_t s);
+
+// Number of bounded waits that gave up in the kernels of element type T since
+// the last call, which resets it.  Synchronous (reads device memory).
+template <typename T>
+cudaError_t take_wait_timeouts(unsigned int* count);
 
 }  // namespace ar

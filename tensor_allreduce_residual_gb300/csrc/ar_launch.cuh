@@ -12,6 +12,7 @@
 #include <climits>
 
 #include "ar_kernels.cuh"
+#include "ar_tma.cuh"
 
 namespace ar {
 
@@ -111,9 +112,40 @@ static cudaError_t run_persist(const FusedArgs& a, OneShotShape sh, cudaStream_t
     return cudaGetLastError();
 }
 
+// Persistent blocks fed by bulk copies: sh.tpr consumer threads plus one
+// producer warp, sh.stages ring slots, sh.blocks_per_sm blocks per SM.
+template <typename T, int R_CT, int CPR>
+static cudaError_t run_tma(const FusedArgs& a, OneShotShape sh, cudaStream_t s)
+{
+    auto kernel = k_fused_oneshot_tma<T, R_CT, CPR>;
+    if (sh.tpr > tma_max_consumers(CPR))
+        return cudaErrorInvalidValue;
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, sh.smem_bytes);
+    int dev = 0, sms = 0;
+    if (e == cudaSuccess)
+        e = cudaGetDevice(&dev);
+    if (e == cudaSuccess)
+        e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess)
+        return e;
+    const long long slots = static_cast<long long>(sms) * sh.blocks_per_sm;
+    const unsigned grid = static_cast<unsigned>(a.tokens < slots ? a.tokens : slots);
+    kernel<<<grid, sh.tpr + 32, sh.smem_bytes, s>>>(a, sh.stages);
+    return cudaGetLastError();
+}
+
 template <typename T, int R_CT>
 static cudaError_t oneshot_packed(const FusedArgs& a, OneShotShape sh, cudaStream_t s)
 {
+    if (sh.mode == kTma) {
+        switch (sh.vpt) {
+        case 1: return run_tma<T, R_CT, 1>(a, sh, s);
+        case 2: return run_tma<T, R_CT, 2>(a, sh, s);
+        case 4: return run_tma<T, R_CT, 4>(a, sh, s);
+        case 8: return run_tma<T, R_CT, 8>(a, sh, s);
+        default: return cudaErrorInvalidValue;
+        }
+    }
     if constexpr (R_CT > 0) {
         if (sh.mode == kPersistent) {
             switch (sh.vpt) {
@@ -171,10 +203,24 @@ cudaError_t launch_fused_twoshot(const FusedArgs& a, bool packed, cudaStream_t s
     }
 }
 
+template <typename T>
+cudaError_t take_wait_timeouts(unsigned int* count)
+{
+    unsigned int v = 0;
+    cudaError_t e = cudaMemcpyFromSymbol(&v, g_wait_timeouts, sizeof(v));
+    if (e == cudaSuccess && v != 0) {
+        const unsigned int zero = 0;
+        e = cudaMemcpyToSymbol(g_wait_timeouts, &zero, sizeof(zero));
+    }
+    *count = v;
+    return e;
+}
+
 }  // namespace ar
 
 #define AR_INSTANTIATE_LAUNCHERS(T)                                                                   \
     template cudaError_t ar::launch_sum<T>(const ar::SumArgs&, bool, int, cudaStream_t);              \
     template cudaError_t ar::launch_fused_oneshot<T>(const ar::FusedArgs&, bool, ar::OneShotShape,    \
                                                      cudaStream_t);                                   \
-    template cudaError_t ar::launch_fused_twoshot<T>(const ar::FusedArgs&, bool, cudaStream_t);
+    template cudaError_t ar::launch_fused_twoshot<T>(const ar::FusedArgs&, bool, cudaStream_t);     \
+    template cudaError_t ar::take_wait_timeouts<T>(unsigned int*);

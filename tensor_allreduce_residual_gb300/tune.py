@@ -1,6 +1,6 @@
 """Measures the fused path's launch choices and writes the AUTO table.
 
-    python -m tensor_allreduce_residual_gb300.tune sweep results.jsonl
+    python -m tensor_allreduce_residual_gb300.tune sweep results.jsonl [--cases A,B] [--shapes S1,S2] [--tokens T1,T2]
     python -m tensor_allreduce_residual_gb300.tune table results.jsonl
 
 `sweep` times every one-shot shape (units per thread x where the row is kept
@@ -30,7 +30,8 @@ CASES = [
     ("R8_bf16_H8192", 8, "bf16", 8192, False, [1, 8, 32, 64, 256, 512, 1024, 2048, 4096, 8192]),
 ]
 SHAPES = ([f"{v}:{m}:{e}" for v in (1, 2, 4, 8) for m in (0, 1) for e in (0, 1)]
-          + [f"{v}:2:{e}" for v in (2, 4) for e in (0, 1)])
+          + [f"{v}:2:{e}" for v in (2, 4) for e in (0, 1)]
+          + [f"{v}:3:{e}:{b}" for v in (1, 2, 4, 8) for e in (0, 1) for b in (1, 2)])
 
 
 def _graph_time(torch, fn, n=10, reps=5):
@@ -56,7 +57,7 @@ def _graph_time(torch, fn, n=10, reps=5):
     return statistics.median(ts)
 
 
-def _measure(strategy: str, shape: str, out):
+def _measure(strategy: str, shape: str, out, cases=None, token_filter=None):
     """Runs in a child process (AR_ONESHOT_SHAPE already set)."""
     sys.path.insert(0, ROOT)
     import torch
@@ -65,7 +66,11 @@ def _measure(strategy: str, shape: str, out):
     import workloads
     torch.cuda.set_device(0)
     for name, R, dtype, H, has_bias, tokens in CASES:
+        if cases and name not in cases:
+            continue
         for T in tokens:
+            if token_filter and T not in token_filter:
+                continue
             f = workloads.fused_inputs(R, T, H, dtype, partial_dist=("N", 0.0, 1.0 / R),
                                        residual_dist=("N", 0.0, 4.0),
                                        bias_dist=("N", 0.0, 0.02) if has_bias else None,
@@ -81,22 +86,25 @@ def _measure(strategy: str, shape: str, out):
                 continue
             rec = {"case": name, "R": R, "esize": workloads.ELEM_SIZE[dtype], "units_row": H * workloads.ELEM_SIZE[dtype] // 16,
                    "T": T, "strategy": strategy, "shape": shape, "us": round(us, 3)}
+            if ar.ar_device_status() != ar.AR_OK:
+                raise RuntimeError(f"{strategy} {shape} T={T}: a kernel gave up a bounded wait")
             out.write(json.dumps(rec) + "\n")
             out.flush()
             del f, o, r, ws
             torch.cuda.empty_cache()
 
 
-def sweep(path: str):
+def sweep(path: str, cases=None, shapes=None, tokens=None):
     with open(path, "w") as out:
-        runs = [("TWOSHOT", "-")] + [("ONESHOT", s) for s in SHAPES]
+        runs = [("TWOSHOT", "-")] + [("ONESHOT", s) for s in (shapes or SHAPES)]
         for strategy, shape in runs:
             env = dict(os.environ)
             env.pop("AR_ONESHOT_SHAPE", None)
             if shape != "-":
                 env["AR_ONESHOT_SHAPE"] = shape
+            extra = [",".join(cases or []), ",".join(str(t) for t in (tokens or []))]
             res = subprocess.run([sys.executable, "-m", "tensor_allreduce_residual_gb300.tune", "_child",
-                                  strategy, shape], cwd=ROOT, env=env, capture_output=True, text=True)
+                                  strategy, shape, *extra], cwd=ROOT, env=env, capture_output=True, text=True)
             if res.returncode != 0:
                 raise RuntimeError(f"sweep child {strategy} {shape} failed:\n{res.stderr[-2000:]}")
             out.write(res.stdout)
@@ -121,17 +129,20 @@ def table(path: str):
         for i, (T, r) in enumerate(items):
             tmax = T if i + 1 < len(items) else 2147483647
             if r["strategy"] == "TWOSHOT":
-                lines.append(f"    {{{esize}, {R}, {units}, {tmax}, 2, 0, 0, 0}},  // {r['case']} T={T}: "
+                lines.append(f"    {{{esize}, {R}, {units}, {tmax}, 2, 0, 0, 0, 1}},  // {r['case']} T={T}: "
                              f"two-shot {r['us']} us")
             else:
-                v, m, e = (int(x) for x in r["shape"].split(":"))
-                lines.append(f"    {{{esize}, {R}, {units}, {tmax}, 1, {v}, {m}, {e}}},  // {r['case']} T={T}: "
+                parts = [int(x) for x in r["shape"].split(":")]
+                v, m = parts[0], parts[1]
+                e = parts[2] if len(parts) > 2 else 0
+                b = parts[3] if len(parts) > 3 else 1
+                lines.append(f"    {{{esize}, {R}, {units}, {tmax}, 1, {v}, {m}, {e}, {b}}},  // {r['case']} T={T}: "
                              f"one-shot {r['us']} us")
     header = open(TABLE).read()
     start = header.index("static const AutoEntry kAutoTable[] = {")
     end = header.index("};", start)
     body = "static const AutoEntry kAutoTable[] = {\n" + "\n".join(lines) + \
-        "\n    {0, 0, 0, 0, 0, 0, 0, 0},  // sentinel\n"
+        "\n    {0, 0, 0, 0, 0, 0, 0, 0, 0},  // sentinel\n"
     header = header[:start] + body + header[end:]
     header = header.replace("// No measured entries yet: every shape takes the rule in ar_api.cu.\n", "")
     with open(TABLE, "w") as f:
@@ -142,9 +153,15 @@ def table(path: str):
 if __name__ == "__main__":
     cmd = sys.argv[1] if len(sys.argv) > 1 else ""
     if cmd == "_child":
-        _measure(sys.argv[2], sys.argv[3], sys.stdout)
+        cases = [c for c in sys.argv[4].split(",") if c] if len(sys.argv) > 4 else None
+        toks = [int(t) for t in sys.argv[5].split(",") if t] if len(sys.argv) > 5 else None
+        _measure(sys.argv[2], sys.argv[3], sys.stdout, cases, toks)
     elif cmd == "sweep":
-        sweep(sys.argv[2])
+        # sweep OUT [--cases a,b] [--shapes s1,s2] [--tokens t1,t2]
+        opts = dict(zip(sys.argv[3::2], sys.argv[4::2]))
+        sweep(sys.argv[2], cases=[c for c in opts.get("--cases", "").split(",") if c] or None,
+              shapes=[c for c in opts.get("--shapes", "").split(",") if c] or None,
+              tokens=[int(t) for t in opts.get("--tokens", "").split(",") if t] or None)
     elif cmd == "table":
         table(sys.argv[2])
     else:

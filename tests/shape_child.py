@@ -42,6 +42,13 @@ def main():
     # more rows than resident blocks: persistent blocks stride over rows
     big = workloads.tp_prefill(tokens=3000, seed=5)
     check(big, rows=[0, 1, 151, 152, 999, 1500, 2047, 2048, 2998, 2999])
+    # rows of 1000 vectors: the last chunk of each row is ragged
+    check(workloads.fused_inputs(8, 37, 8000, "bf16", partial_dist=("N", 0.0, 0.125), residual_dist=("N", 0.0, 4.0),
+                                 bias_dist=("N", 0.0, 0.02), weight_dist=("N", 1.0, 0.05), eps=1e-6, seed=6))
+    # a rank count without a compile-time specialisation
+    check(workloads.fused_inputs(3, 21, 4096, "fp16", partial_dist=("N", 0.0, 0.3), residual_dist=("N", 0.0, 4.0),
+                                 bias_dist=("N", 0.0, 0.02), weight_dist=("N", 1.0, 0.05), eps=1e-5, seed=7))
+    assert ar.ar_device_status() == ar.AR_OK, "a kernel gave up a bounded wait"
     print("shape ok")
 
 

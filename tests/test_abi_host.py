@@ -37,7 +37,7 @@ def _declared_functions():
 def test_header_declares_the_expected_entry_points():
     names = _declared_functions()
     for want in ["ar_version", "ar_strerror", "ar_workspace_size", "ar_workspace_size_rows", "ar_sum",
-                 "ar_residual_rmsnorm", "ar_allreduce", "ar_query_strategy"]:
+                 "ar_residual_rmsnorm", "ar_allreduce", "ar_query_strategy", "ar_query_launch", "ar_device_status"]:
         assert want in names, names
 
 
@@ -52,7 +52,8 @@ def test_library_exports_every_declared_symbol(L):
 
 def test_version_and_strerror(L):
     assert ar.ar_version() == 10000
-    for code in (ar.AR_OK, ar.AR_ERR_INVALID_ARG, ar.AR_ERR_UNSUPPORTED, ar.AR_ERR_WORKSPACE, ar.AR_ERR_CUDA):
+    for code in (ar.AR_OK, ar.AR_ERR_INVALID_ARG, ar.AR_ERR_UNSUPPORTED, ar.AR_ERR_WORKSPACE, ar.AR_ERR_CUDA,
+                 ar.AR_ERR_TIMEOUT):
         assert ar.ar_strerror(code) and ar.ar_strerror(code) != "unknown status code"
     assert ar.ar_strerror(12345) == "unknown status code"
 
@@ -198,3 +199,50 @@ def test_query_strategy(L):
         ar.ar_query_strategy(2, 100, 64, ar.AR_FP32)                 # not a whole number of rows
     with pytest.raises(ar.ARError):
         ar.ar_query_strategy(0, 100, 10, ar.AR_FP32)
+
+
+def test_launch_plan_struct_layout_matches_c(tmp_path):
+    src = tmp_path / "plan.c"
+    fields = [name for name, _ in ar.ArLaunchPlan._fields_]
+    src.write_text(f'''
+#include <stdio.h>
+#include <stddef.h>
+#include "{HEADER}"
+int main(void) {{
+  printf("%zu{" %zu" * len(fields)}\\n", sizeof(ar_launch_plan){"".join(f", offsetof(ar_launch_plan, {f})" for f in fields)});
+  return 0;
+}}''')
+    exe = tmp_path / "plan"
+    subprocess.run(["gcc", "-std=c11", str(src), "-o", str(exe)], check=True)
+    got = [int(v) for v in subprocess.run([str(exe)], capture_output=True, text=True, check=True).stdout.split()]
+    P = ar.ArLaunchPlan
+    assert got == [ctypes.sizeof(P)] + [getattr(P, f).offset for f in fields]
+
+
+def test_query_launch(L):
+    # TP prefill, R=8 bf16 8192 x 8192: the measured table picks the bulk-copy-fed persistent kernel
+    p = ar.ar_query_launch(8, 8192, 8192, ar.AR_BF16)
+    assert p["strategy"] == ar.AR_ONESHOT and p["kernel"] == 4 and p["kernel_name"] == "k_fused_oneshot_tma"
+    assert p["threads_per_block"] == p["threads_per_row"] + 32 and p["threads_per_row"] % 32 == 0
+    assert p["stages"] >= 2 and p["blocks_per_sm"] >= 1
+    assert p["smem_bytes"] * p["blocks_per_sm"] <= 228 * 1024
+    # decode: a register-resident one-shot kernel
+    p = ar.ar_query_launch(2, 4096, 1, ar.AR_FP16)
+    assert p["strategy"] == ar.AR_ONESHOT and p["kernel"] == 1 and p["stages"] == 0
+    assert p["threads_per_row"] * p["units_per_thread"] * 8 >= 4096
+    # forced two-shot
+    p = ar.ar_query_launch(8, 8192, 64, ar.AR_BF16, "TWOSHOT")
+    assert p["strategy"] == ar.AR_TWOSHOT and p["kernel"] == 5
+    # the AUTO answer agrees with ar_query_strategy
+    for R, H, T, dt in [(8, 8192, 1, ar.AR_BF16), (8, 8192, 8192, ar.AR_BF16), (2, 4096, 32, ar.AR_FP16),
+                        (2, 64, 4, ar.AR_FP32)]:
+        s, w = ar.ar_query_strategy(R, H * T, H, dt)
+        p = ar.ar_query_launch(R, H, T, dt)
+        assert p["strategy"] == s and (s != ar.AR_ONESHOT or (p["threads_per_row"] + 31) // 32 == w)
+    # errors, nothing launched
+    plan = ar.ArLaunchPlan()
+    assert L.ar_query_launch(0, 64, 4, ar.AR_FP32, ar.AR_AUTO, ctypes.byref(plan)) == ar.AR_ERR_INVALID_ARG
+    assert L.ar_query_launch(2, 64, 4, ar.AR_FP32, ar.AR_AUTO, None) == ar.AR_ERR_INVALID_ARG
+    assert L.ar_query_launch(2, 64, 4, 9, ar.AR_AUTO, ctypes.byref(plan)) == ar.AR_ERR_UNSUPPORTED
+    assert L.ar_query_launch(2, 64, 4, ar.AR_FP32, ar.AR_NCCL, ctypes.byref(plan)) == ar.AR_ERR_UNSUPPORTED
+    assert L.ar_query_launch(2, 65536 * 2, 4, ar.AR_FP32, ar.AR_ONESHOT, ctypes.byref(plan)) == ar.AR_ERR_UNSUPPORTED

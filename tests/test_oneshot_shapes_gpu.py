@@ -1,6 +1,7 @@
-"""Every one-shot launch shape (registers / shared memory / persistent blocks,
-units per thread, residual_out written before or after the row barrier) gives
-oracle-parity results.  Each shape runs in a child process because the shape
+"""Every one-shot launch shape (registers / shared memory / persistent blocks /
+persistent blocks fed by bulk copies, units per thread, residual_out written
+before or after the row barrier) gives oracle-parity results, and no kernel
+gives up a bounded wait.  Each shape runs in a child process because the shape
 override is read once per process."""
 import os
 import subprocess
@@ -11,7 +12,9 @@ import pytest
 pytestmark = pytest.mark.gpu
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-SHAPES = ["1:0:1", "2:0:0", "4:0:1", "8:0:0", "1:1:0", "2:1:1", "4:1:0", "8:1:1", "2:2:1", "4:2:0", "4:2:1"]
+SHAPES = ["1:0:1", "2:0:0", "4:0:1", "8:0:0", "1:1:0", "2:1:1", "4:1:0", "8:1:1", "2:2:1", "4:2:0", "4:2:1",
+          # persistent blocks fed by bulk copies: chunks per row : 3 : early : blocks per SM
+          "1:3:0", "2:3:1", "4:3:0", "4:3:1:2", "8:3:0:2", "8:3:1"]
 
 
 @pytest.mark.parametrize("shape", SHAPES)
