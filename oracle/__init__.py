@@ -57,6 +57,8 @@ def _load():
             ctypes.POINTER(vp), ctypes.c_int, vp, vp, vp, ctypes.c_float,
             ctypes.c_int, ctypes.c_int, ctypes.c_int, vp, vp, vp, vp]
         lib.or_residual_rmsnorm.restype = None
+        lib.or_rmsnorm.argtypes = [vp, vp, ctypes.c_float, ctypes.c_int, ctypes.c_int, ctypes.c_int, vp, vp]
+        lib.or_rmsnorm.restype = None
         _lib = lib
     return _lib
 
@@ -128,3 +130,15 @@ def residual_rmsnorm(partials, bias, residual, weight, eps: float, dtype: str):
         hidden, tokens, _CODES[dtype], out.data_ptr(), res_out.data_ptr(),
         inv.ctypes.data, xrow.ctypes.data)
     return out, res_out, inv[:tokens]
+
+
+def rmsnorm(x, weight, eps: float, dtype: str):
+    """RMSNorm of [tokens, hidden] rows on their own: (out, inv_rms per row as float64 numpy)."""
+    tokens, hidden = x.shape
+    _check(x, dtype, tokens * hidden, "x")
+    _check(weight, dtype, hidden, "weight")
+    out = torch.empty((tokens, hidden), dtype=_TORCH[dtype])
+    inv = np.zeros(max(tokens, 1), dtype=np.float64)
+    _load().or_rmsnorm(x.data_ptr(), weight.data_ptr(), ctypes.c_float(eps), hidden, tokens, _CODES[dtype],
+                       out.data_ptr(), inv.ctypes.data)
+    return out, inv[:tokens]

@@ -27,6 +27,11 @@
  *         out_j = x_j * inv * weight_j,   residual_out_j = x_j
  *     bias is added once (not per rank) and may be absent; eps is the
  *     float value the caller passes, widened exactly to double.
+ *   - or_rmsnorm: the row normalisation on its own ("allreduce.d2",
+ *     rms_norm_kernel_launcher -> rms_norm_kernel, the second phase of the
+ *     two-shot fused route and the norm after a plain all-reduce):
+ *         out_j = x_j / sqrt( (sum_j x_j^2) / H + eps ) * weight_j
+ *     with the same reading of the formula as above.
  *
  * Formats (the pages' PackedOn16Bytes unions in "type.d2" name float and
  * half; bfloat16 is added beside them):
@@ -207,5 +212,26 @@ void or_residual_rmsnorm(const void* const* partials, int R, const void* bias,
             store(residual_out, row + j, dtype, xrow[j]);
             store(out, row + j, dtype, xrow[j] * inv * w);
         }
+    }
+}
+
+/* RMSNorm of a row-major [tokens, hidden] tensor x on its own:
+ * out[t,j] = x[t,j] * (1 / sqrt(mean_j x[t,j]^2 + eps)) * weight[j], the
+ * factor in binary64, rounded once.  inv_rms as in or_residual_rmsnorm. */
+void or_rmsnorm(const void* x, const void* weight, float eps, int hidden, int tokens,
+                int dtype, void* out, double* inv_rms)
+{
+    for (int t = 0; t < tokens; ++t) {
+        size_t row = (size_t)t * (size_t)hidden;
+        double sumsq = 0.0;
+        for (int j = 0; j < hidden; ++j) {
+            double v = load(x, row + j, dtype);
+            sumsq += v * v;
+        }
+        double inv = 1.0 / sqrt(sumsq / (double)hidden + (double)eps);
+        if (inv_rms)
+            inv_rms[t] = inv;
+        for (int j = 0; j < hidden; ++j)
+            store(out, row + j, dtype, load(x, row + j, dtype) * inv * load(weight, (size_t)j, dtype));
     }
 }

@@ -72,7 +72,7 @@ int next_pow2(int v)
 // Bulk-copy-fed persistent shape (mode kTma): vpt = chunks per row, one
 // consumer thread per vector of a chunk (a multiple of 32), and as many ring
 // slots as the shared memory of `blocks_per_sm` blocks per SM allows.
-bool tma_shape(int units_row, int vpt, int R, int blocks_per_sm, OneShotShape* sh)
+bool tma_shape(int units_row, int vpt, int R, int blocks_per_sm, int max_stages, OneShotShape* sh)
 {
     if (!(vpt == 1 || vpt == 2 || vpt == 4 || vpt == 8) || blocks_per_sm < 1 || blocks_per_sm > 4)
         return false;
@@ -82,7 +82,7 @@ bool tma_shape(int units_row, int vpt, int R, int blocks_per_sm, OneShotShape* s
     int budget = ar::kSmemPerSM / blocks_per_sm - ar::kSmemReservedPerBlock;
     if (budget > ar::kSmemPerBlockMax)
         budget = ar::kSmemPerBlockMax;
-    int stages = ar::kTmaMaxStages;
+    int stages = max_stages >= ar::kTmaMinStages && max_stages < ar::kTmaMaxStages ? max_stages : ar::kTmaMaxStages;
     while (stages >= ar::kTmaMinStages && ar::tma_smem_bytes(R, nc, stages) > static_cast<size_t>(budget))
         --stages;
     if (stages < ar::kTmaMinStages)
@@ -98,10 +98,10 @@ bool tma_shape(int units_row, int vpt, int R, int blocks_per_sm, OneShotShape* s
 }
 
 bool oneshot_shape(int units_row, int vpt, int lanes, bool packed, int mode, int R, OneShotShape* sh,
-                   int blocks_per_sm = 1)
+                   int blocks_per_sm = 1, int max_stages = 0)
 {
     if (mode == ar::kTma)
-        return packed && tma_shape(units_row, vpt, R, blocks_per_sm, sh);
+        return packed && tma_shape(units_row, vpt, R, blocks_per_sm, max_stages, sh);
     const int max_vpt = packed ? ar::kMaxVPTVec : ar::kMaxVPTScalar;
     const bool stage = mode != ar::kRegisters;
     if (vpt < 1 || vpt > max_vpt || (stage && (!packed || vpt > ar::kMaxVPTVec)))
@@ -156,14 +156,16 @@ const ar::AutoEntry* table_lookup(int esize, int R, int units_row, int tokens)
 }
 
 // Measurement override of the one-shot shape: AR_ONESHOT_SHAPE="vpt:mode",
-// "vpt:mode:early" or "vpt:mode:early:blocks_per_sm" (e.g. "4:1", "2:0:1",
-// "4:3:0:2") replaces the table and the rule for every packed call.  Read
+// "vpt:mode:early", "vpt:mode:early:blocks_per_sm" or
+// "vpt:mode:early:blocks_per_sm:max_stages" (e.g. "4:1", "2:0:1", "4:3:0:2",
+// "4:3:1:1:3") replaces the table and the rule for every packed call.  Read
 // once per process; used to sweep shapes when building the AUTO table.
 struct ShapeOverride {
     int vpt = 0;
     int mode = 0;
     int early = 0;
     int blocks_per_sm = 1;
+    int max_stages = 0;
 };
 
 const ShapeOverride& shape_override()
@@ -171,13 +173,14 @@ const ShapeOverride& shape_override()
     static const ShapeOverride ov = [] {
         ShapeOverride o;
         if (const char* env = std::getenv("AR_ONESHOT_SHAPE")) {
-            int v = 0, st = 0, early = 0, bps = 1;
-            const int got = std::sscanf(env, "%d:%d:%d:%d", &v, &st, &early, &bps);
+            int v = 0, st = 0, early = 0, bps = 1, stages = 0;
+            const int got = std::sscanf(env, "%d:%d:%d:%d:%d", &v, &st, &early, &bps, &stages);
             if (got >= 2 && v > 0 && st >= 0 && st <= ar::kTma) {
                 o.vpt = v;
                 o.mode = st;
                 o.early = got >= 3 && early != 0;
-                o.blocks_per_sm = got == 4 && bps > 0 ? bps : 1;
+                o.blocks_per_sm = got >= 4 && bps > 0 ? bps : 1;
+                o.max_stages = got == 5 && stages > 0 ? stages : 0;
             }
         }
         return o;
@@ -201,6 +204,7 @@ FusedPlan plan_fused(int esize, int R, int hidden, int tokens, bool packed, int 
     int mode = ar::kRegisters;
     int early = 1;
     int bps = 1;
+    int max_stages = 0;
     int auto_strategy = AR_ONESHOT;
     if (packed) {
         if (const ar::AutoEntry* e = table_lookup(esize, R, units_row, tokens)) {
@@ -210,6 +214,7 @@ FusedPlan plan_fused(int esize, int R, int hidden, int tokens, bool packed, int 
                 mode = e->mode;
                 early = e->early;
                 bps = e->blocks_per_sm > 0 ? e->blocks_per_sm : 1;
+                max_stages = e->max_stages;
             }
         }
         const ShapeOverride& ov = shape_override();
@@ -218,9 +223,10 @@ FusedPlan plan_fused(int esize, int R, int hidden, int tokens, bool packed, int 
             mode = ov.mode;
             early = ov.early;
             bps = ov.blocks_per_sm;
+            max_stages = ov.max_stages;
         }
     }
-    p.oneshot_ok = oneshot_shape(units_row, vpt, lanes, packed, mode, R, &p.shape, bps);
+    p.oneshot_ok = oneshot_shape(units_row, vpt, lanes, packed, mode, R, &p.shape, bps, max_stages);
     if (!p.oneshot_ok)  // the chosen shape does not fit this row: the rule's shape
         p.oneshot_ok = oneshot_shape(units_row, rule_vpt(units_row, tokens, lanes, packed), lanes,
                                      packed, ar::kRegisters, R, &p.shape);

@@ -21,31 +21,32 @@ struct AutoEntry {
     int vpt;         // one-shot units per thread
     int mode;        // one-shot OneShotMode: 0 registers, 1 shared memory, 2 persistent, 3 bulk-copy ring
     int early;       // one-shot: 1 = write residual_out before the row barrier
-    int blocks_per_sm = 1;  // one-shot mode 3: resident blocks per SM
+    int blocks_per_sm = 1;  // one-shot mode 3: blocks per SM the grid is sized for
+    int max_stages = 0;     // one-shot mode 3: ring slots per block at most (0: as many as fit)
 };
 
 static const AutoEntry kAutoTable[] = {
-    {2, 2, 512, 1, 1, 1, 0, 1, 1},  // tp_decode_R2_fp16_H4096 T=1: one-shot 2.493 us
-    {2, 2, 512, 2, 1, 1, 0, 1, 1},  // tp_decode_R2_fp16_H4096 T=2: one-shot 2.522 us
-    {2, 2, 512, 4, 1, 2, 0, 1, 1},  // tp_decode_R2_fp16_H4096 T=4: one-shot 2.784 us
-    {2, 2, 512, 8, 1, 1, 0, 0, 1},  // tp_decode_R2_fp16_H4096 T=8: one-shot 2.755 us
-    {2, 2, 512, 16, 1, 1, 0, 1, 1},  // tp_decode_R2_fp16_H4096 T=16: one-shot 2.918 us
-    {2, 2, 512, 32, 1, 1, 0, 1, 1},  // tp_decode_R2_fp16_H4096 T=32: one-shot 2.739 us
-    {2, 2, 512, 64, 1, 1, 0, 1, 1},  // tp_decode_R2_fp16_H4096 T=64: one-shot 2.762 us
-    {2, 2, 512, 256, 1, 2, 0, 1, 1},  // tp_decode_R2_fp16_H4096 T=256: one-shot 3.318 us
-    {2, 2, 512, 1024, 1, 2, 0, 1, 1},  // tp_decode_R2_fp16_H4096 T=1024: one-shot 6.112 us
-    {2, 2, 512, 2147483647, 1, 1, 0, 1, 1},  // tp_decode_R2_fp16_H4096 T=8192: one-shot 52.349 us
-    {2, 8, 1024, 1, 1, 2, 0, 1, 1},  // R8_bf16_H8192 T=1: one-shot 3.971 us
-    {2, 8, 1024, 8, 1, 2, 0, 1, 1},  // R8_bf16_H8192 T=8: one-shot 4.218 us
-    {2, 8, 1024, 32, 1, 2, 0, 1, 1},  // R8_bf16_H8192 T=32: one-shot 4.16 us
-    {2, 8, 1024, 64, 1, 2, 0, 1, 1},  // R8_bf16_H8192 T=64: one-shot 4.211 us
-    {2, 8, 1024, 256, 1, 2, 0, 1, 1},  // R8_bf16_H8192 T=256: one-shot 6.016 us
-    {2, 8, 1024, 512, 1, 2, 3, 1, 1},  // R8_bf16_H8192 T=512: one-shot 12.717 us
-    {2, 8, 1024, 1024, 1, 4, 1, 0, 1},  // R8_bf16_H8192 T=1024: one-shot 29.632 us
-    {2, 8, 1024, 2048, 1, 4, 3, 1, 2},  // R8_bf16_H8192 T=2048: one-shot 58.032 us
-    {2, 8, 1024, 4096, 1, 4, 3, 1, 2},  // R8_bf16_H8192 T=4096: one-shot 110.438 us
-    {2, 8, 1024, 2147483647, 1, 4, 3, 1, 2},  // R8_bf16_H8192 T=8192: one-shot 213.098 us
-    {0, 0, 0, 0, 0, 0, 0, 0, 0},  // sentinel
+    {2, 2, 512, 1, 1, 1, 0, 1, 1, 0},  // tp_decode_R2_fp16_H4096 T=1: one-shot 2.493 us
+    {2, 2, 512, 2, 1, 1, 0, 1, 1, 0},  // tp_decode_R2_fp16_H4096 T=2: one-shot 2.522 us
+    {2, 2, 512, 4, 1, 2, 0, 1, 1, 0},  // tp_decode_R2_fp16_H4096 T=4: one-shot 2.784 us
+    {2, 2, 512, 8, 1, 1, 0, 0, 1, 0},  // tp_decode_R2_fp16_H4096 T=8: one-shot 2.755 us
+    {2, 2, 512, 16, 1, 1, 0, 1, 1, 0},  // tp_decode_R2_fp16_H4096 T=16: one-shot 2.918 us
+    {2, 2, 512, 32, 1, 1, 0, 1, 1, 0},  // tp_decode_R2_fp16_H4096 T=32: one-shot 2.739 us
+    {2, 2, 512, 64, 1, 1, 0, 1, 1, 0},  // tp_decode_R2_fp16_H4096 T=64: one-shot 2.762 us
+    {2, 2, 512, 256, 1, 2, 0, 1, 1, 0},  // tp_decode_R2_fp16_H4096 T=256: one-shot 3.318 us
+    {2, 2, 512, 1024, 1, 2, 0, 1, 1, 0},  // tp_decode_R2_fp16_H4096 T=1024: one-shot 6.112 us
+    {2, 2, 512, 2147483647, 1, 1, 0, 1, 1, 0},  // tp_decode_R2_fp16_H4096 T=8192: one-shot 52.349 us
+    {2, 8, 1024, 1, 1, 2, 0, 1, 1, 0},  // R8_bf16_H8192 T=1: one-shot 3.971 us
+    {2, 8, 1024, 8, 1, 2, 0, 1, 1, 0},  // R8_bf16_H8192 T=8: one-shot 4.218 us
+    {2, 8, 1024, 32, 1, 2, 0, 1, 1, 0},  // R8_bf16_H8192 T=32: one-shot 4.16 us
+    {2, 8, 1024, 64, 1, 2, 0, 1, 1, 0},  // R8_bf16_H8192 T=64: one-shot 4.211 us
+    {2, 8, 1024, 256, 1, 2, 0, 1, 1, 0},  // R8_bf16_H8192 T=256: one-shot 6.016 us
+    {2, 8, 1024, 512, 1, 2, 3, 1, 1, 0},  // R8_bf16_H8192 T=512: one-shot 12.717 us
+    {2, 8, 1024, 1024, 1, 4, 1, 0, 1, 0},  // R8_bf16_H8192 T=1024: one-shot 29.632 us
+    {2, 8, 1024, 2048, 1, 2, 3, 1, 1, 2},  // R8_bf16_H8192 T=2048: one-shot 55.418 us
+    {2, 8, 1024, 4096, 1, 2, 3, 1, 1, 2},  // R8_bf16_H8192 T=4096: one-shot 106.141 us
+    {2, 8, 1024, 2147483647, 1, 2, 3, 1, 1, 2},  // R8_bf16_H8192 T=8192: one-shot 207.725 us
+    {0, 0, 0, 0, 0, 0, 0, 0, 0, 0},  // sentinel
 };
 
 }  // namespace ar

@@ -129,20 +129,21 @@ def table(path: str):
         for i, (T, r) in enumerate(items):
             tmax = T if i + 1 < len(items) else 2147483647
             if r["strategy"] == "TWOSHOT":
-                lines.append(f"    {{{esize}, {R}, {units}, {tmax}, 2, 0, 0, 0, 1}},  // {r['case']} T={T}: "
+                lines.append(f"    {{{esize}, {R}, {units}, {tmax}, 2, 0, 0, 0, 1, 0}},  // {r['case']} T={T}: "
                              f"two-shot {r['us']} us")
             else:
                 parts = [int(x) for x in r["shape"].split(":")]
                 v, m = parts[0], parts[1]
                 e = parts[2] if len(parts) > 2 else 0
                 b = parts[3] if len(parts) > 3 else 1
-                lines.append(f"    {{{esize}, {R}, {units}, {tmax}, 1, {v}, {m}, {e}, {b}}},  // {r['case']} T={T}: "
+                st = parts[4] if len(parts) > 4 else 0
+                lines.append(f"    {{{esize}, {R}, {units}, {tmax}, 1, {v}, {m}, {e}, {b}, {st}}},  // {r['case']} T={T}: "
                              f"one-shot {r['us']} us")
     header = open(TABLE).read()
     start = header.index("static const AutoEntry kAutoTable[] = {")
     end = header.index("};", start)
     body = "static const AutoEntry kAutoTable[] = {\n" + "\n".join(lines) + \
-        "\n    {0, 0, 0, 0, 0, 0, 0, 0, 0},  // sentinel\n"
+        "\n    {0, 0, 0, 0, 0, 0, 0, 0, 0, 0},  // sentinel\n"
     header = header[:start] + body + header[end:]
     header = header.replace("// No measured entries yet: every shape takes the rule in ar_api.cu.\n", "")
     with open(TABLE, "w") as f:

@@ -7,7 +7,9 @@
 - the fused op: a hand-computed worked example (tests/golden/hand_h8.json),
   closed forms (H=1 and H=2 rows), the RMS invariant, scale invariance,
   row independence, bias placement, permutation invariance, R=1 identity and
-  the eps=0 special case against numpy's vector norm.
+  the eps=0 special case against numpy's vector norm;
+- the norm on its own (or_rmsnorm): the same worked example, the RMS closed
+  form, numpy's vector norm at eps=0, scale invariance and row permutation.
 """
 import json
 import math
@@ -309,3 +311,53 @@ def test_sum_signed_zero_passthrough(dtype):
     assert torch.all(torch.signbit(one)) and torch.all(torch.signbit(two))
     mixed = oracle.sum([neg, torch.zeros(16, dtype=TD[dtype])], dtype)
     assert not torch.any(torch.signbit(mixed))        # -0 + +0 = +0 (round to nearest)
+
+
+# ---------------------------------------------------------------- the norm on its own
+
+@pytest.mark.parametrize("dtype", ["fp32", "fp16", "bf16"])
+def test_rmsnorm_hand_worked_example_exact(dtype):
+    """The golden rows x (already summed by hand), eps = 1: out and the per-row factor are exact."""
+    d = _golden()
+    out, inv = oracle.rmsnorm(_t(d["expected_residual_out"], dtype), _t(d["weight"], dtype), d["eps"], dtype)
+    assert out.to(torch.float64).tolist() == d["expected_out"]
+    assert inv.tolist() == [0.5, 0.25]
+
+
+def test_rmsnorm_rms_closed_form():
+    """weight = 1: mean(out^2) = ms / (ms + eps) for every row, from tiny to large rows."""
+    T, H, eps = 6, 512, 1e-6
+    g = torch.Generator().manual_seed(31)
+    scales = torch.tensor([1e-4, 3e-4, 1e-3, 1e-2, 1.0, 30.0], dtype=torch.float64)
+    x = (torch.randn(T, H, generator=g, dtype=torch.float64) * scales[:, None]).float().contiguous()
+    out, _ = oracle.rmsnorm(x, torch.ones(H, dtype=torch.float32), eps, "fp32")
+    xv, yv = x.double().numpy(), out.double().numpy()
+    ms = (xv ** 2).mean(axis=1)
+    ratio = ms / (ms + float(np.float32(eps)))
+    assert np.allclose((yv ** 2).mean(axis=1), ratio, rtol=1e-6, atol=0)
+    assert ratio.min() < 0.1 and ratio.max() > 0.999
+
+
+def test_rmsnorm_eps_zero_is_vector_normalisation():
+    """eps = 0, weight = 1: out = x / ||x||_2 * sqrt(H), with numpy's norm."""
+    g = torch.Generator().manual_seed(32)
+    x = torch.randn(7, 96, generator=g).contiguous()
+    out, _ = oracle.rmsnorm(x, torch.ones(96), 0.0, "fp32")
+    xv = x.double().numpy()
+    want = xv / np.linalg.norm(xv, axis=1, keepdims=True) * math.sqrt(96)
+    assert np.allclose(out.double().numpy(), want, rtol=2.0 ** -22, atol=0)
+
+
+@pytest.mark.parametrize("dtype", ["fp32", "fp16", "bf16"])
+def test_rmsnorm_scale_and_row_permutation(dtype):
+    """x * 2^k with eps * 4^k leaves out unchanged; permuting rows permutes out."""
+    g = torch.Generator().manual_seed(33)
+    x = torch.randn(9, 40, generator=g, dtype=torch.float64).to(TD[dtype]).contiguous()
+    w = (1.0 + 0.1 * torch.randn(40, generator=g, dtype=torch.float64)).to(TD[dtype]).contiguous()
+    eps = float(np.float32(1e-3))
+    o1, _ = oracle.rmsnorm(x, w, eps, dtype)
+    o2, _ = oracle.rmsnorm((x.to(torch.float64) * 8).to(TD[dtype]).contiguous(), w, eps * 64, dtype)
+    assert torch.equal(o1.view(torch.uint8), o2.view(torch.uint8))
+    perm = torch.tensor([4, 0, 8, 2, 6, 1, 7, 3, 5])
+    o3, _ = oracle.rmsnorm(x[perm].contiguous(), w, eps, dtype)
+    assert torch.equal(o3.view(torch.uint8), o1[perm].contiguous().view(torch.uint8))
