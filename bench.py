@@ -244,20 +244,22 @@ def run_ours(args, rank, world, local_rank):
                 "traffic": traffic, "algorithmic_bytes_per_launch": bytes_call,
                 "launch_ms_mean": round(mean_launch_ms, 5), "launch_ms_median": round(statistics.median(per_step), 5)}
 
-    # End to end through the same C-ABI call: host (pinned) inputs copied in and
-    # both outputs copied back inside the timed region, every step.
-    host_in = [t.cpu().pin_memory() for t in parts + [resid, weight, bias]]
-    dev_in = parts + [resid, weight, bias]
+    # End to end through the C ABI on HOST buffers: every step,
+    # ar_residual_rmsnorm_host copies that step's inputs from pinned host
+    # memory, runs the fused kernels and copies both outputs back, in chunks
+    # of 512 rows with the copies overlapping the kernels.  Timed on the
+    # stream until the outputs are in host memory.
+    host_parts = [t.cpu().pin_memory() for t in parts]
+    host_res, host_w, host_b = (t.cpu().pin_memory() for t in (resid, weight, bias))
     host_out = [torch.empty(out.shape, dtype=out.dtype).pin_memory() for _ in range(2)]
-    h2d = sum(t.numel() * t.element_size() for t in host_in)
+    chunk = 512
+    staging = torch.empty(ar.ar_host_staging_size(R, HIDDEN, chunk, ar.AR_BF16), dtype=torch.uint8, device=dev)
+    h2d = sum(t.numel() * t.element_size() for t in host_parts + [host_res, host_w, host_b])
     d2h = sum(t.numel() * t.element_size() for t in host_out)
 
     def e2e_step():
-        for d, h in zip(dev_in, host_in):
-            d.copy_(h, non_blocking=True)
-        step()
-        host_out[0].copy_(out, non_blocking=True)
-        host_out[1].copy_(res_out, non_blocking=True)
+        ar.ar_residual_rmsnorm_host(host_parts, host_res, host_w, EPS, staging, host_out[0], host_out[1],
+                                    bias=host_b, chunk_tokens=chunk, strategy=args.strategy, stream=stream)
 
     for _ in range(2):
         e2e_step()
@@ -272,8 +274,9 @@ def run_ours(args, rank, world, local_rank):
     e2e = {"value": round(bytes_call * world * args.e2e_steps / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": args.e2e_steps,
            "us_per_call": round(e2e_ms * 1e3 / args.e2e_steps, 1),
-           "note": "pinned host inputs copied in and both outputs copied out inside the timed region"}
-    del host_in, host_out
+           "note": ("ar_residual_rmsnorm_host on pinned host buffers: inputs copied in and both outputs copied "
+                    f"out inside the timed region, {chunk}-row chunks pipelined against the kernels")}
+    del host_parts, host_out, staging
 
     extras = None
     if not args.no_extras and rank == 0:
@@ -366,6 +369,28 @@ def run_extras(ar, torch, workloads, parts, resid, weight, bias, out, res_out, w
             parts, resid, weight, EPS, bias=bias, out=out, residual_out=res_out, intermediate=ws,
             strategy=s), stream, 100)
         ex[f"prefill_{s}"] = {"us_per_call": round(ms * 1e3, 2), "GBps": round(bytes_call / ms / 1e6, 1)}
+    # The unfused route (the pages' "all-reduce, then norm"): ar_sum into a
+    # temporary, then the residual + bias + norm call with that sum as its one
+    # partial.  It moves (R+1)n s + 4n s + 2H s bytes against the fused
+    # (R+3)n s + 2H s; GBps_effective counts the fused call's bytes.
+    tmp = torch.empty_like(resid)
+
+    def unfused():
+        ar.ar_sum(parts, out=tmp)
+        ar.ar_residual_rmsnorm([tmp], resid, weight, EPS, bias=bias, out=out, residual_out=res_out, intermediate=ws)
+
+    ms = _time_calls(torch, unfused, stream, 50)
+    T_, H_ = resid.shape
+    moved = (len(parts) + 1) * T_ * H_ * 2 + 4 * T_ * H_ * 2 + 2 * H_ * 2
+    ex["prefill_unfused_sum_then_norm"] = {
+        "us_per_call": round(ms * 1e3, 2), "GBps_effective": round(bytes_call / ms / 1e6, 1),
+        "bytes_moved": moved, "GBps_moved": round(moved / ms / 1e6, 1),
+        "fused_speedup": round(ms * 1e3 / ex["prefill_ONESHOT"]["us_per_call"], 3)}
+    ms = _time_calls(torch, lambda: ar.ar_rmsnorm(res_out, weight, EPS, out=out), stream, 50)
+    nb = 2 * T_ * H_ * 2 + H_ * 2
+    ex["prefill_rmsnorm_alone"] = {"us_per_call": round(ms * 1e3, 2), "bytes": nb, "GBps": round(nb / ms / 1e6, 1)}
+    del tmp
+
     flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
     dec = {}
     for T in (1, 8, 32):

@@ -171,6 +171,67 @@ int ar_residual_rmsnorm(const void* const* partials, int R, const void* bias,
                         int dtype, int strategy, ar_stream_t stream);
 
 /*
+ * ar_rmsnorm -- out[t,j] = x[t,j] / sqrt(mean_j(x[t,:]^2) + eps) * weight[j],
+ * the row normalisation on its own: rms_norm_kernel_launcher ->
+ * rms_norm_kernel of "allreduce.d2", which the pages run after a plain
+ * all-reduce and as the second phase of the two-shot fused route.  With
+ * ar_sum before it this is the unfused route of the fused call.
+ *
+ *   x       device [tokens, hidden]; out may equal x (in place)
+ *   weight  device [hidden]
+ *   eps     float, >= 0
+ *   out     device [tokens, hidden]
+ * Each row is held in registers between its sum of squares and its output,
+ * so hidden <= 16384.  Same accumulation (fp32, fixed reduction tree) and
+ * alignment rules as ar_residual_rmsnorm.  tokens == 0 launches nothing.
+ * Errors: AR_ERR_INVALID_ARG (hidden < 1, tokens < 0, NULL pointer, eps < 0
+ *         or not finite), AR_ERR_UNSUPPORTED (unknown dtype, hidden > 16384),
+ *         AR_ERR_CUDA.
+ */
+int ar_rmsnorm(const void* x, const void* weight, float eps, int hidden, int tokens, void* out,
+               int dtype, ar_stream_t stream);
+
+/*
+ * ar_host_staging_size -- bytes of device staging that
+ * ar_residual_rmsnorm_host needs for chunks of `chunk_tokens` rows: two
+ * buffers of (R + 3) [chunk_tokens, hidden] tensors plus a two-shot
+ * workspace each, then weight and bias (all 256-byte aligned).  0 for an
+ * invalid shape.
+ */
+size_t ar_host_staging_size(int R, int hidden, int chunk_tokens, int dtype);
+
+/*
+ * ar_residual_rmsnorm_host -- ar_residual_rmsnorm on tensors in HOST memory
+ * (partials, bias, residual, weight, out, residual_out: same shapes and
+ * meaning), for data that is not resident on the device.  The call copies
+ * the rows in chunks of chunk_tokens rows into `staging` (device memory of
+ * at least ar_host_staging_size(R, hidden, chunk_tokens, dtype) bytes,
+ * 256-byte aligned, owned by the caller), runs the fused kernels on each
+ * chunk on `stream`, and copies the outputs back, with the copies of chunk
+ * i+1 and i-1 overlapping the kernels of chunk i (two staging buffers, two
+ * copy streams).  No pages' counterpart: the plugin of "All Reduce Plugin"
+ * works on device tensors only.
+ *
+ * Asynchronous like every call here: it returns once everything is queued.
+ * Work queued on `stream` before the call happens before the first copy,
+ * and work queued on `stream` after it sees the outputs in host memory (so
+ * cudaStreamSynchronize(stream) waits for them).  Host buffers must stay
+ * valid and unchanged until then; they should be pinned (cudaHostAlloc /
+ * cudaHostRegister), otherwise the copies do not overlap.  The first call
+ * on a device creates two streams and a few events there and keeps them
+ * for the life of the process.  Calls that may run at the same time need
+ * separate staging buffers.
+ * Errors: as ar_residual_rmsnorm, plus AR_ERR_INVALID_ARG (chunk_tokens < 1,
+ *         NULL staging) and AR_ERR_WORKSPACE (staging too small or not
+ *         256-byte aligned).
+ */
+int ar_residual_rmsnorm_host(const void* const* partials, int R, const void* bias,
+                             const void* residual, const void* weight, float eps,
+                             int hidden, int tokens, void* out, void* residual_out,
+                             void* staging, size_t staging_bytes, int chunk_tokens,
+                             int dtype, int strategy, ar_stream_t stream);
+
+/*
  * ar_params -- one structure holding every argument, after AllReduceParams
  * (elts_total, peer_comm_buffer_ptrs, local_output_buffer_ptr) and its
  * AllReduceFusionParams member (bias_buffer, residual_buffer, hidden_size,

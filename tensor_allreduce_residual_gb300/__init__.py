@@ -100,6 +100,10 @@ def lib() -> ctypes.CDLL:
     L.ar_residual_rmsnorm_noalloc.argtypes = [pvp, i, vp, vp, vp, ctypes.c_float, i, i, vp, vp, i, vp]
     L.ar_residual_rmsnorm_noalloc.restype = i
     L.ar_device_status.argtypes, L.ar_device_status.restype = [], i
+    L.ar_rmsnorm.argtypes, L.ar_rmsnorm.restype = [vp, vp, ctypes.c_float, i, i, vp, i, vp], i
+    L.ar_host_staging_size.argtypes, L.ar_host_staging_size.restype = [i, i, i, i], sz
+    L.ar_residual_rmsnorm_host.argtypes = [pvp, i, vp, vp, vp, ctypes.c_float, i, i, vp, vp, vp, sz, i, i, i, vp]
+    L.ar_residual_rmsnorm_host.restype = i
     L.ar_query_launch.argtypes = [i, i, i, i, i, ctypes.POINTER(ArLaunchPlan)]
     L.ar_query_launch.restype = i
     _lib = L
@@ -273,6 +277,59 @@ def ar_residual_rmsnorm_noalloc(partials: Sequence[torch.Tensor], residual: torc
         _dev_ptr(weight, "weight"), ctypes.c_float(eps), hidden, tokens, _dev_ptr(out, "out"),
         _dev_ptr(residual_out, "residual_out"), dtype_code(residual.dtype), _stream_handle(stream))
     _check("ar_residual_rmsnorm_noalloc", status)
+    return out, residual_out
+
+
+def ar_rmsnorm(x: torch.Tensor, weight: torch.Tensor, eps: float, out: Optional[torch.Tensor] = None,
+               stream=None) -> torch.Tensor:
+    """out = RMSNorm of the [tokens, hidden] rows of x, times weight (out may be x)."""
+    if x.dim() != 2:
+        raise ValueError("x must be [tokens, hidden]")
+    tokens, hidden = x.shape
+    if weight.numel() != hidden or weight.dtype != x.dtype:
+        raise ValueError("weight must be [hidden] of x's dtype")
+    if out is None:
+        out = torch.empty_like(x)
+    elif out.numel() != x.numel() or out.dtype != x.dtype:
+        raise ValueError("out must match x in size and dtype")
+    _check("ar_rmsnorm", lib().ar_rmsnorm(_dev_ptr(x, "x"), _dev_ptr(weight, "weight"), ctypes.c_float(eps), hidden,
+                                          tokens, _dev_ptr(out, "out"), dtype_code(x.dtype), _stream_handle(stream)))
+    return out
+
+
+def ar_host_staging_size(R: int, hidden: int, chunk_tokens: int, dtype) -> int:
+    code = dtype if isinstance(dtype, int) else dtype_code(dtype)
+    return int(lib().ar_host_staging_size(R, hidden, chunk_tokens, code))
+
+
+def _host_ptr(t: Optional[torch.Tensor], what: str) -> Optional[int]:
+    if t is None:
+        return None
+    if t.is_cuda:
+        raise ValueError(f"{what} must be a host (CPU) tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{what} must be contiguous")
+    return t.data_ptr()
+
+
+def ar_residual_rmsnorm_host(partials: Sequence[torch.Tensor], residual: torch.Tensor, weight: torch.Tensor,
+                             eps: float, staging: torch.Tensor, out: torch.Tensor, residual_out: torch.Tensor,
+                             bias: Optional[torch.Tensor] = None, chunk_tokens: int = 512, strategy="AUTO",
+                             stream=None):
+    """The fused call on host (preferably pinned) tensors, copies pipelined through device `staging`.
+
+    Asynchronous: synchronise `stream` before reading out / residual_out.
+    """
+    if residual.dim() != 2:
+        raise ValueError("residual must be [tokens, hidden]")
+    tokens, hidden = residual.shape
+    ptrs = _ptr_array([_host_ptr(p, f"partials[{k}]") for k, p in enumerate(partials)])
+    status = lib().ar_residual_rmsnorm_host(
+        ptrs, len(partials), _host_ptr(bias, "bias"), _host_ptr(residual, "residual"), _host_ptr(weight, "weight"),
+        ctypes.c_float(eps), hidden, tokens, _host_ptr(out, "out"), _host_ptr(residual_out, "residual_out"),
+        _dev_ptr(staging, "staging"), staging.numel() * staging.element_size(), chunk_tokens,
+        dtype_code(residual.dtype), _strategy(strategy), _stream_handle(stream))
+    _check("ar_residual_rmsnorm_host", status)
     return out, residual_out
 
 

@@ -17,7 +17,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libar.so")
 
-SOURCES = ["ar_api.cu", "ar_kern_f32.cu", "ar_kern_f16.cu", "ar_kern_bf16.cu", "ar_noalloc.cu"]
+SOURCES = ["ar_api.cu", "ar_kern_f32.cu", "ar_kern_f16.cu", "ar_kern_bf16.cu", "ar_noalloc.cu", "ar_host.cu"]
 HEADERS = ["ar_internal.h", "ar_kernels.cuh", "ar_tma.cuh", "ar_launch.cuh", "ar_auto_table.h"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

@@ -72,7 +72,8 @@ int next_pow2(int v)
 // Bulk-copy-fed persistent shape (mode kTma): vpt = chunks per row, one
 // consumer thread per vector of a chunk (a multiple of 32), and as many ring
 // slots as the shared memory of `blocks_per_sm` blocks per SM allows.
-bool tma_shape(int units_row, int vpt, int R, int blocks_per_sm, int max_stages, OneShotShape* sh)
+// `inputs` = tensors streamed through the ring: R partials plus the residual.
+bool tma_shape(int units_row, int vpt, int inputs, int blocks_per_sm, int max_stages, OneShotShape* sh)
 {
     if (!(vpt == 1 || vpt == 2 || vpt == 4 || vpt == 8) || blocks_per_sm < 1 || blocks_per_sm > 4)
         return false;
@@ -83,7 +84,7 @@ bool tma_shape(int units_row, int vpt, int R, int blocks_per_sm, int max_stages,
     if (budget > ar::kSmemPerBlockMax)
         budget = ar::kSmemPerBlockMax;
     int stages = max_stages >= ar::kTmaMinStages && max_stages < ar::kTmaMaxStages ? max_stages : ar::kTmaMaxStages;
-    while (stages >= ar::kTmaMinStages && ar::tma_smem_bytes(R, nc, stages) > static_cast<size_t>(budget))
+    while (stages >= ar::kTmaMinStages && ar::tma_smem_bytes(inputs, nc, stages) > static_cast<size_t>(budget))
         --stages;
     if (stages < ar::kTmaMinStages)
         return false;
@@ -91,7 +92,7 @@ bool tma_shape(int units_row, int vpt, int R, int blocks_per_sm, int max_stages,
     sh->vpt = vpt;
     sh->rows = 1;
     sh->mode = ar::kTma;
-    sh->smem_bytes = static_cast<int>(ar::tma_smem_bytes(R, nc, stages));
+    sh->smem_bytes = static_cast<int>(ar::tma_smem_bytes(inputs, nc, stages));
     sh->stages = stages;
     sh->blocks_per_sm = blocks_per_sm;
     return true;
@@ -101,7 +102,7 @@ bool oneshot_shape(int units_row, int vpt, int lanes, bool packed, int mode, int
                    int blocks_per_sm = 1, int max_stages = 0)
 {
     if (mode == ar::kTma)
-        return packed && tma_shape(units_row, vpt, R, blocks_per_sm, max_stages, sh);
+        return packed && tma_shape(units_row, vpt, R + 1, blocks_per_sm, max_stages, sh);
     const int max_vpt = packed ? ar::kMaxVPTVec : ar::kMaxVPTScalar;
     const bool stage = mode != ar::kRegisters;
     if (vpt < 1 || vpt > max_vpt || (stage && (!packed || vpt > ar::kMaxVPTVec)))
@@ -245,6 +246,9 @@ int twoshot_nchunk(int units_row)
 }
 
 size_t round256(size_t b) { return (b + 255) / 256 * 256; }
+
+// ar_rmsnorm takes the bulk-copy-fed kernel from this many rows on.
+constexpr int kNormTmaMinTokens = 1024;
 
 }  // namespace
 
@@ -398,6 +402,49 @@ int ar_residual_rmsnorm(const void* const* partials, int R, const void* bias, co
         if (plan.strategy == AR_ONESHOT)
             return ar::launch_fused_oneshot<T>(a, packed, plan.shape, s);
         return ar::launch_fused_twoshot<T>(a, packed, s);
+    }));
+}
+
+int ar_rmsnorm(const void* x, const void* weight, float eps, int hidden, int tokens, void* out, int dtype,
+               ar_stream_t stream)
+{
+    if (hidden < 1 || tokens < 0)
+        return AR_ERR_INVALID_ARG;
+    const int esize = esize_of(dtype);
+    if (esize == 0)
+        return AR_ERR_UNSUPPORTED;
+    if (!std::isfinite(eps) || eps < 0.0f)
+        return AR_ERR_INVALID_ARG;
+    if (tokens == 0)
+        return AR_OK;
+    if (x == nullptr || weight == nullptr || out == nullptr)
+        return AR_ERR_INVALID_ARG;
+    const int lanes = 16 / esize;
+    const bool packed = hidden % lanes == 0 && aligned16(x) && aligned16(weight) && aligned16(out);
+    const int units_row = packed ? hidden / lanes : hidden;
+    OneShotShape sh{};
+    // Many rows: the bulk-copy-fed persistent kernel, about 128 KB of copies
+    // in flight per SM (x is the only streamed input).  Otherwise, and for
+    // rows it cannot hold, the register-resident row kernel.
+    bool tma = packed && tokens >= kNormTmaMinTokens &&
+               tma_shape(units_row, units_row <= 512 ? 1 : (units_row <= 1024 ? 2 : 4), 1, 1, 16, &sh);
+    if (!tma && !oneshot_shape(units_row, rule_vpt(units_row, tokens, packed ? lanes : 1, packed),
+                               packed ? lanes : 1, packed, ar::kRegisters, 1, &sh))
+        return AR_ERR_UNSUPPORTED;
+    FusedArgs a{};
+    a.partials[0] = x;
+    a.weight = weight;
+    a.out = out;
+    a.R = 1;
+    a.hidden = hidden;
+    a.tokens = tokens;
+    a.units_row = units_row;
+    a.eps = eps;
+    a.early_residual = 0;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    return status_of(by_dtype(dtype, [&](auto tag) {
+        using T = decltype(tag);
+        return tma ? ar::launch_rmsnorm_tma<T>(a, sh, s) : ar::launch_rmsnorm<T>(a, packed, sh, s);
     }));
 }
 

@@ -50,10 +50,10 @@ struct SumArgs {
 struct FusedArgs {
     const void* partials[kMaxRanks];
     const void* bias;      // nullable
-    const void* residual;
+    const void* residual;  // nullable for the norm on its own
     const void* weight;
     void* out;
-    void* residual_out;
+    void* residual_out;    // nullable for the norm on its own
     float* sumsq;          // two-shot workspace: [tokens, nchunk] fp32
     int R;
     int hidden;
@@ -109,12 +109,13 @@ constexpr int kSmemPerBlockMax = 227 * 1024;  // opt-in dynamic shared memory of
 constexpr int kSmemPerSM = 228 * 1024;        // shared memory of one SM
 constexpr int kSmemReservedPerBlock = 1024;   // taken by the runtime from each resident block
 
-// Shared memory of one kTma block: `stages` ring slots of (R + 1) * nc
-// 16-byte vectors, then a full and an empty barrier per slot (8 bytes each),
-// then the row-reduction scratch, [2][32] floats.
-__host__ __device__ constexpr size_t tma_smem_bytes(int R, int nc, int stages)
+// Shared memory of one kTma block: `stages` ring slots of `inputs` * nc
+// 16-byte vectors (inputs = the R partials, plus the residual when there is
+// one), then a full and an empty barrier per slot (8 bytes each), then the
+// row-reduction scratch, [2][32] floats.
+__host__ __device__ constexpr size_t tma_smem_bytes(int inputs, int nc, int stages)
 {
-    return static_cast<size_t>(stages) * (R + 1) * nc * 16 + static_cast<size_t>(stages) * 16 + 2 * 32 * 4;
+    return static_cast<size_t>(stages) * inputs * nc * 16 + static_cast<size_t>(stages) * 16 + 2 * 32 * 4;
 }
 
 // Launchers, explicitly instantiated for float, __half and __nv_bfloat16 in
@@ -127,6 +128,16 @@ cudaError_t launch_fused_oneshot(const FusedArgs& a, bool packed, OneShotShape s
 
 template <typename T>
 cudaError_t launch_fused_twoshot(const FusedArgs& a, bool packed, cudaStream_t s);
+
+// RMSNorm of a.partials[0] rows into a.out (register-resident rows, shape.mode
+// must be kRegisters).
+template <typename T>
+cudaError_t launch_rmsnorm(const FusedArgs& a, bool packed, OneShotShape shape, cudaStream_t s);
+
+// The same through the bulk-copy-fed persistent kernel (shape.mode == kTma):
+// a.partials[0] is x, a.R == 1, no bias, residual or residual_out.
+template <typename T>
+cudaError_t launch_rmsnorm_tma(const FusedArgs& a, OneShotShape shape, cudaStream_t s);
 
 // Number of bounded waits that gave up in the kernels of element type T since
 // the last call, which resets it.  Synchronous (reads device memory).

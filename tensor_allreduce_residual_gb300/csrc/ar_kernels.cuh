@@ -522,6 +522,59 @@ k_fused_oneshot_persist(const FusedArgs a)
 }
 
 // ---------------------------------------------------------------------------
+// RMSNorm of x rows on its own (rms_norm_kernel_launcher -> rms_norm_kernel,
+// "allreduce.d2": the norm that follows a plain all-reduce).  Same layout
+// as the register-resident one-shot kernel: `tpr` threads own a row, each
+// keeps VPT units of x in registers across the row reduction, so x is read
+// once and out written once.  x is a.partials[0]; out may alias x.
+// ---------------------------------------------------------------------------
+template <typename T, bool PACKED, int VPT>
+__global__ void __launch_bounds__(oneshot_max_threads(VPT * Unit<T, PACKED>::L))
+k_rmsnorm(const FusedArgs a, const int tpr)
+{
+    using U = Unit<T, PACKED>;
+    constexpr int L = U::L;
+    __shared__ float red[32];
+
+    const int lane_row = threadIdx.x & (tpr - 1);
+    const int row = blockIdx.x * (blockDim.x / tpr) + static_cast<int>(threadIdx.x) / tpr;
+    const bool row_ok = row < a.tokens;
+    const uint64_t row_off = static_cast<uint64_t>(row) * a.units_row;
+
+    float x[VPT][L];
+    typename U::raw wv[VPT];
+    float ss = 0.0f;
+#pragma unroll
+    for (int k = 0; k < VPT; ++k) {
+        const int j = lane_row + k * tpr;
+#pragma unroll
+        for (int l = 0; l < L; ++l)
+            x[k][l] = 0.0f;
+        if (row_ok && j < a.units_row) {
+            U::to_float(U::load(a.partials[0], row_off + j), x[k]);
+            wv[k] = U::load_cached(a.weight, j);
+#pragma unroll
+            for (int l = 0; l < L; ++l)
+                ss = fmaf(x[k][l], x[k][l], ss);
+        }
+    }
+    ss = row_sum(ss, tpr, red);
+    const float inv = inv_rms(ss, a.hidden, a.eps);
+#pragma unroll
+    for (int k = 0; k < VPT; ++k) {
+        const int j = lane_row + k * tpr;
+        if (row_ok && j < a.units_row) {
+            float w[L], y[L];
+            U::to_float(wv[k], w);
+#pragma unroll
+            for (int l = 0; l < L; ++l)
+                y[l] = x[k][l] * inv * w[l];
+            U::store(a.out, row_off + j, y);
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
 // A6: two-shot fused phase 1 (twoShotAllReduceKernel in the fused route of
 // AllReduceNormKernelLaunch, "allreduce.d2").  Block b owns chunk
 // (b % nchunk) of row (b / nchunk): it writes the pre-norm sum to

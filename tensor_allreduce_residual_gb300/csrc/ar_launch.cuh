@@ -175,6 +175,48 @@ cudaError_t launch_fused_oneshot(const FusedArgs& a, bool packed, OneShotShape s
     }
 }
 
+template <typename T, bool PACKED, int VPT>
+static cudaError_t run_rmsnorm(const FusedArgs& a, OneShotShape sh, cudaStream_t s)
+{
+    const unsigned grid = static_cast<unsigned>((a.tokens + sh.rows - 1) / sh.rows);
+    k_rmsnorm<T, PACKED, VPT><<<grid, sh.tpr * sh.rows, 0, s>>>(a, sh.tpr);
+    return cudaGetLastError();
+}
+
+template <typename T, bool PACKED>
+static cudaError_t rmsnorm_vpt(const FusedArgs& a, OneShotShape sh, cudaStream_t s)
+{
+    switch (sh.vpt) {
+    case 1: return run_rmsnorm<T, PACKED, 1>(a, sh, s);
+    case 2: return run_rmsnorm<T, PACKED, 2>(a, sh, s);
+    case 4: return run_rmsnorm<T, PACKED, 4>(a, sh, s);
+    case 8: return run_rmsnorm<T, PACKED, 8>(a, sh, s);
+    case 16:
+        if constexpr (!PACKED)
+            return run_rmsnorm<T, PACKED, 16>(a, sh, s);
+        return cudaErrorInvalidValue;
+    default: return cudaErrorInvalidValue;
+    }
+}
+
+template <typename T>
+cudaError_t launch_rmsnorm(const FusedArgs& a, bool packed, OneShotShape sh, cudaStream_t s)
+{
+    return packed ? rmsnorm_vpt<T, true>(a, sh, s) : rmsnorm_vpt<T, false>(a, sh, s);
+}
+
+template <typename T>
+cudaError_t launch_rmsnorm_tma(const FusedArgs& a, OneShotShape sh, cudaStream_t s)
+{
+    switch (sh.vpt) {
+    case 1: return run_tma<T, 1, 1>(a, sh, s);
+    case 2: return run_tma<T, 1, 2>(a, sh, s);
+    case 4: return run_tma<T, 1, 4>(a, sh, s);
+    case 8: return run_tma<T, 1, 8>(a, sh, s);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
 template <typename T, bool PACKED, int R_CT>
 static cudaError_t run_twoshot(const FusedArgs& a, cudaStream_t s)
 {
@@ -223,4 +265,6 @@ cudaError_t take_wait_timeouts(unsigned int* count)
     template cudaError_t ar::launch_fused_oneshot<T>(const ar::FusedArgs&, bool, ar::OneShotShape,    \
                                                      cudaStream_t);                                   \
     template cudaError_t ar::launch_fused_twoshot<T>(const ar::FusedArgs&, bool, cudaStream_t);     \
-    template cudaError_t ar::take_wait_timeouts<T>(unsigned int*);
+    template cudaError_t ar::take_wait_timeouts<T>(unsigned int*);                                  \
+    template cudaError_t ar::launch_rmsnorm<T>(const ar::FusedArgs&, bool, ar::OneShotShape, cudaStream_t);      \
+    template cudaError_t ar::launch_rmsnorm_tma<T>(const ar::FusedArgs&, ar::OneShotShape, cudaStream_t);

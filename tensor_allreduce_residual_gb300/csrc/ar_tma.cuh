@@ -11,6 +11,9 @@
 // ring holds ~200 KB per SM in flight, and loads for later rows continue
 // while the consumers wait at a row barrier.
 //
+// The residual input and the residual_out output are optional (both absent
+// for the norm on its own: R = 1 partial holding x, no bias).
+//
 // Block = NC consumer threads (NC = vectors per chunk, a multiple of 32) plus
 // one producer warp.  A row of units_row 16-byte vectors is split into
 // ceil(units_row / NC) <= CPR chunks; consumer thread t owns vector
@@ -129,9 +132,11 @@ k_fused_oneshot_tma(const FusedArgs a, const int stages)
     using U = Unit<T, true>;
     constexpr int L = U::L;
     const int R = R_CT > 0 ? R_CT : a.R;
+    const bool has_res = a.residual != nullptr;
+    const int inputs = R + (has_res ? 1 : 0);           // streamed tensors
     const int nc = static_cast<int>(blockDim.x) - 32;   // consumer threads = vectors per chunk
     const int nchunk = (a.units_row + nc - 1) / nc;     // <= CPR (checked by the host)
-    const size_t slot_vecs = static_cast<size_t>(R + 1) * nc;
+    const size_t slot_vecs = static_cast<size_t>(inputs) * nc;
 
     extern __shared__ __align__(128) unsigned char smem[];
     uint4* ring = reinterpret_cast<uint4*>(smem);
@@ -143,7 +148,7 @@ k_fused_oneshot_tma(const FusedArgs a, const int stages)
     if (tid == 0) {
         for (int s = 0; s < stages; ++s) {
             mbar_init(&full[s], 1);
-            mbar_init(&empty[s], static_cast<uint32_t>(nc));
+            mbar_init(&empty[s], static_cast<uint32_t>(nc / 32));  // one arrival per consumer warp
         }
         fence_mbar_init();
     }
@@ -167,13 +172,14 @@ k_fused_oneshot_tma(const FusedArgs a, const int stages)
                 }
                 const int j0 = c * nc;
                 const uint32_t bytes = static_cast<uint32_t>(min(nc, a.units_row - j0)) * 16u;
-                mbar_arrive_expect_tx(&full[s], bytes * static_cast<uint32_t>(R + 1));
+                mbar_arrive_expect_tx(&full[s], bytes * static_cast<uint32_t>(inputs));
                 uint4* dst = ring + static_cast<size_t>(s) * slot_vecs;
                 for (int r = 0; r < R; ++r)
                     bulk_copy_g2s(dst + static_cast<size_t>(r) * nc,
                                   static_cast<const uint4*>(a.partials[r]) + row_off + j0, bytes, &full[s]);
-                bulk_copy_g2s(dst + static_cast<size_t>(R) * nc,
-                              static_cast<const uint4*>(a.residual) + row_off + j0, bytes, &full[s]);
+                if (has_res)
+                    bulk_copy_g2s(dst + static_cast<size_t>(R) * nc,
+                                  static_cast<const uint4*>(a.residual) + row_off + j0, bytes, &full[s]);
                 ++it;
                 if (++s == stages) {
                     s = 0;
@@ -239,15 +245,21 @@ k_fused_oneshot_tma(const FusedArgs a, const int stages)
                         U::to_float(bv[c], t);
                         add_lanes<L>(x[c], t);
                     }
-                    U::to_float(src[static_cast<size_t>(R) * nc], t);
-                    add_lanes<L>(x[c], t);
-                    if (a.early_residual)
+                    if (has_res) {
+                        U::to_float(src[static_cast<size_t>(R) * nc], t);
+                        add_lanes<L>(x[c], t);
+                    }
+                    if (a.early_residual && a.residual_out != nullptr)
                         U::store(a.residual_out, row_off + j, x[c]);
 #pragma unroll
                     for (int l = 0; l < L; ++l)
                         ss = fmaf(x[c][l], x[c][l], ss);
                 }
-                mbar_arrive(&empty[s]);  // this thread is done with the slot
+                // The warp is done with the slot: its lanes' shared-memory reads
+                // are ordered before lane 0's (releasing) arrival by __syncwarp.
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(&empty[s]);
                 if (++s == stages) {
                     s = 0;
                     ph ^= 1u;
@@ -274,7 +286,7 @@ k_fused_oneshot_tma(const FusedArgs a, const int stages)
         for (int c = 0; c < CPR; ++c) {
             const int j = c * nc + tid;
             if (c < nchunk && j < a.units_row) {
-                if (!a.early_residual)
+                if (!a.early_residual && a.residual_out != nullptr)
                     U::store(a.residual_out, row_off + j, x[c]);
                 float w[L], y[L];
                 U::to_float(wv[c], w);

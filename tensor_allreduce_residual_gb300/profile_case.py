@@ -3,6 +3,7 @@
     python -m tensor_allreduce_residual_gb300.profile_case fused \
         --R 8 --tokens 1024 --hidden 8192 --dtype bf16 --strategy ONESHOT --calls 3
     python -m tensor_allreduce_residual_gb300.profile_case sum --R 4 --n 33554432 --dtype fp16
+    python -m tensor_allreduce_residual_gb300.profile_case rmsnorm --tokens 8192 --hidden 8192 --dtype bf16
 
 Inputs are the seeded synthetic workloads (drawn on the device), the calls go
 through the C ABI, and nothing is timed or checked: the point is a short,
@@ -22,7 +23,7 @@ if ROOT not in sys.path:
 
 def main(argv=None) -> int:
     p = argparse.ArgumentParser(description="run one library case for a profiler")
-    p.add_argument("op", choices=["fused", "sum"])
+    p.add_argument("op", choices=["fused", "sum", "rmsnorm"])
     p.add_argument("--R", type=int, default=8)
     p.add_argument("--tokens", type=int, default=1024)
     p.add_argument("--hidden", type=int, default=8192)
@@ -45,6 +46,11 @@ def main(argv=None) -> int:
         s = workloads.sum_inputs(a.R, a.n, a.dtype, ("U", -1.0, 1.0), seed=0, device="cuda")
         out = torch.empty_like(s.partials[0])
         call = lambda: ar.ar_sum(s.partials, out=out, strategy=a.strategy)  # noqa: E731
+    elif a.op == "rmsnorm":
+        x = workloads.draw(("N", 0.0, 4.0), a.tokens * a.hidden, a.dtype, 0, 100, "cuda").view(a.tokens, a.hidden)
+        w = workloads.draw(("N", 1.0, 0.05), a.hidden, a.dtype, 0, 300, "cuda")
+        out = torch.empty_like(x)
+        call = lambda: ar.ar_rmsnorm(x, w, 1e-6, out=out)  # noqa: E731
     else:
         f = workloads.fused_inputs(a.R, a.tokens, a.hidden, a.dtype, partial_dist=("N", 0.0, 1.0 / a.R),
                                    residual_dist=("N", 0.0, 4.0),

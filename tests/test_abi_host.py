@@ -37,7 +37,8 @@ def _declared_functions():
 def test_header_declares_the_expected_entry_points():
     names = _declared_functions()
     for want in ["ar_version", "ar_strerror", "ar_workspace_size", "ar_workspace_size_rows", "ar_sum",
-                 "ar_residual_rmsnorm", "ar_allreduce", "ar_query_strategy", "ar_query_launch", "ar_device_status"]:
+                 "ar_residual_rmsnorm", "ar_allreduce", "ar_query_strategy", "ar_query_launch", "ar_device_status",
+                 "ar_rmsnorm", "ar_host_staging_size", "ar_residual_rmsnorm_host"]:
         assert want in names, names
 
 
@@ -246,3 +247,43 @@ def test_query_launch(L):
     assert L.ar_query_launch(2, 64, 4, 9, ar.AR_AUTO, ctypes.byref(plan)) == ar.AR_ERR_UNSUPPORTED
     assert L.ar_query_launch(2, 64, 4, ar.AR_FP32, ar.AR_NCCL, ctypes.byref(plan)) == ar.AR_ERR_UNSUPPORTED
     assert L.ar_query_launch(2, 65536 * 2, 4, ar.AR_FP32, ar.AR_ONESHOT, ctypes.byref(plan)) == ar.AR_ERR_UNSUPPORTED
+
+
+def test_rmsnorm_argument_errors(L):
+    def call(x=FAKE, w=FAKE + 4096, eps=1e-6, H=64, T=4, out=FAKE + 8192, dtype=ar.AR_FP32):
+        return L.ar_rmsnorm(x, w, ctypes.c_float(eps), H, T, out, dtype, None)
+    assert call(H=0) == ar.AR_ERR_INVALID_ARG
+    assert call(T=-1) == ar.AR_ERR_INVALID_ARG
+    assert call(eps=-1.0) == ar.AR_ERR_INVALID_ARG
+    assert call(eps=float("nan")) == ar.AR_ERR_INVALID_ARG
+    assert call(x=None) == ar.AR_ERR_INVALID_ARG
+    assert call(w=None) == ar.AR_ERR_INVALID_ARG
+    assert call(out=None) == ar.AR_ERR_INVALID_ARG
+    assert call(dtype=4) == ar.AR_ERR_UNSUPPORTED
+    assert call(H=16385, dtype=ar.AR_BF16) == ar.AR_ERR_UNSUPPORTED      # beyond the register-resident row
+    assert call(H=16385 * 4, dtype=ar.AR_FP32) == ar.AR_ERR_UNSUPPORTED
+    assert call(T=0, x=None, out=None) == ar.AR_OK                       # empty: nothing launched
+
+
+def test_host_staging_size_and_errors(L):
+    # two buffers of (R + 3) chunk tensors + a workspace each, then weight and bias
+    R, H, C = 8, 8192, 512
+    chunk = C * H * 2
+    ws = L.ar_workspace_size_rows(R, H, C, ar.AR_BF16)
+    assert L.ar_host_staging_size(R, H, C, ar.AR_BF16) == 2 * ((R + 3) * chunk + ws) + 2 * H * 2
+    assert L.ar_host_staging_size(0, H, C, ar.AR_BF16) == 0
+    assert L.ar_host_staging_size(R, H, 0, ar.AR_BF16) == 0
+    assert L.ar_host_staging_size(R, H, C, 7) == 0
+
+    def call(R=2, T=4, H=64, chunk=2, staging=FAKE, nbytes=1 << 30, residual=FAKE + 1, ptrs=None, dtype=ar.AR_FP32):
+        return L.ar_residual_rmsnorm_host(ptrs if ptrs is not None else _ptrs(R), R, None, residual, FAKE + 2,
+                                          ctypes.c_float(1e-6), H, T, FAKE + 3, FAKE + 4, staging, nbytes, chunk,
+                                          dtype, ar.AR_AUTO, None)
+    assert call(R=0) == ar.AR_ERR_INVALID_ARG
+    assert call(chunk=0) == ar.AR_ERR_INVALID_ARG
+    assert call(staging=None) == ar.AR_ERR_INVALID_ARG
+    assert call(residual=None) == ar.AR_ERR_INVALID_ARG
+    assert call(dtype=9) == ar.AR_ERR_UNSUPPORTED
+    assert call(nbytes=100) == ar.AR_ERR_WORKSPACE
+    assert call(staging=FAKE + 16) == ar.AR_ERR_WORKSPACE        # not 256-byte aligned
+    assert call(T=0) == ar.AR_OK

@@ -1,0 +1,73 @@
+"""ar_residual_rmsnorm_host: the fused call on host tensors, copies pipelined
+through device staging.  Its outputs must match the oracle like the device
+call's, residual_out bit for bit with the device call, for row counts that
+split into several chunks with a ragged last one, a single chunk, and chunk
+sizes of one row."""
+import pytest
+import torch
+
+import oracle
+import tensor_allreduce_residual_gb300 as ar
+import workloads
+from tests import tolerance as tol
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def cuda_library():
+    assert torch.cuda.is_available()
+    torch.cuda.set_device(0)
+    ar.lib()
+
+
+def _pin(t):
+    return None if t is None else t.contiguous().pin_memory()
+
+
+def _run_host(inp, chunk, strategy="AUTO"):
+    parts = [_pin(p.reshape(inp.tokens, inp.hidden)) for p in inp.partials]
+    res, w, b = _pin(inp.residual), _pin(inp.weight), _pin(inp.bias)
+    out = torch.empty_like(res).pin_memory()
+    rout = torch.empty_like(res).pin_memory()
+    staging = torch.empty(ar.ar_host_staging_size(inp.R, inp.hidden, min(chunk, inp.tokens),
+                                                  ar.dtype_code(res.dtype)), dtype=torch.uint8, device="cuda")
+    ar.ar_residual_rmsnorm_host(parts, res, w, inp.eps, staging, out, rout, bias=b, chunk_tokens=chunk,
+                                strategy=strategy)
+    torch.cuda.current_stream().synchronize()
+    return out, rout
+
+
+def _check(inp, out, rout):
+    ref = oracle.residual_rmsnorm(inp.partials, inp.bias, inp.residual, inp.weight, inp.eps, inp.dtype)
+    terms = [p.reshape(inp.tokens, inp.hidden) for p in inp.partials]
+    if inp.bias is not None:
+        terms.append(inp.bias.expand(inp.tokens, inp.hidden).contiguous())
+    terms.append(inp.residual)
+    tol.check_sum(rout, ref[1], terms, inp.dtype, "residual_out")
+    tol.check_fused_out(out, ref[0], terms, inp.weight, ref[2], inp.dtype, inp.hidden, "out")
+    d_out, d_rout = ar.ar_residual_rmsnorm([p.cuda() for p in inp.partials], inp.residual.cuda(), inp.weight.cuda(),
+                                           inp.eps, bias=None if inp.bias is None else inp.bias.cuda())
+    assert torch.equal(d_rout.cpu().view(torch.uint8), rout.view(torch.uint8))
+
+
+@pytest.mark.parametrize("chunk", [1, 8, 16, 64])
+def test_host_path_chunks(chunk):
+    inp = workloads.fused_inputs(8, 37, 8192, "bf16", partial_dist=("N", 0.0, 0.125), residual_dist=("N", 0.0, 4.0),
+                                 bias_dist=("N", 0.0, 0.02), weight_dist=("N", 1.0, 0.05), eps=1e-6, seed=chunk)
+    _check(inp, *_run_host(inp, chunk))
+
+
+def test_host_path_decode_shape_no_bias_and_strategies():
+    inp = workloads.tp_decode(5, seed=3)
+    for s in ("ONESHOT", "TWOSHOT", "AUTO"):
+        _check(inp, *_run_host(inp, 2, s))
+    inp = workloads.decode_r8(9, seed=4)
+    _check(inp, *_run_host(inp, 4))
+
+
+def test_host_path_repeated_calls_share_nothing_stale():
+    a = workloads.tp_prefill(tokens=24, hidden=4096, seed=5)
+    b = workloads.tp_prefill(tokens=24, hidden=4096, seed=6)
+    for inp in (a, b, a):
+        _check(inp, *_run_host(inp, 5))

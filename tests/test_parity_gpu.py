@@ -360,3 +360,55 @@ def test_rms_of_normalised_rows_on_gpu():
         want = ms / (ms + float(np.float32(1e-6)))
         got = (out.double().numpy() ** 2).mean(axis=1)
         assert np.allclose(got, want, rtol=1e-5, atol=0)
+
+
+# ---------------------------------------------------------------- the norm on its own, and the unfused route
+
+def _norm_rows(T, H, dtype, seed, scale=2.0):
+    g = torch.Generator().manual_seed(seed)
+    x = (torch.randn(T, H, generator=g, dtype=torch.float64) * scale).to(TD[dtype]).contiguous()
+    w = (1.0 + 0.05 * torch.randn(H, generator=g, dtype=torch.float64)).to(TD[dtype]).contiguous()
+    return x, w
+
+
+@pytest.mark.parametrize("dtype", ["fp32", "fp16", "bf16"])
+@pytest.mark.parametrize("T,H", [(1, 4096), (7, 8192), (300, 64), (33, 16384), (5, 100), (3, 3), (129, 1024),
+                                 # 1024 rows or more: the bulk-copy-fed kernel (ragged chunks at H=8000)
+                                 (1500, 8192), (1024, 8000), (1100, 1000), (1030, 64), (1024, 16384)])
+def test_rmsnorm_matches_oracle(dtype, T, H):
+    x, w = _norm_rows(T, H, dtype, seed=T * 7 + H)
+    eps = 1e-5
+    out = ar.ar_rmsnorm(x.cuda(), w.cuda(), eps)
+    torch.cuda.synchronize()
+    ref, inv = oracle.rmsnorm(x, w, eps, dtype)
+    tol.check_fused_out(out.cpu(), ref, [x], w, inv, dtype, H, "rmsnorm out")
+
+
+def test_rmsnorm_in_place_and_limits():
+    x, w = _norm_rows(17, 8192, "bf16", seed=3)
+    ref, _ = oracle.rmsnorm(x, w, 1e-6, "bf16")
+    xd = x.cuda()
+    ar.ar_rmsnorm(xd, w.cuda(), 1e-6, out=xd)
+    torch.cuda.synchronize()
+    assert torch.equal(xd.cpu().view(torch.int16), ar.ar_rmsnorm(x.cuda(), w.cuda(), 1e-6).cpu().view(torch.int16))
+    tol.check_fused_out(xd.cpu(), ref, [x], w, oracle.rmsnorm(x, w, 1e-6, "bf16")[1], "bf16", 8192, "in place")
+    big = torch.zeros(1, 16385, dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(ar.ARError) as e:
+        ar.ar_rmsnorm(big, torch.ones(16385, dtype=torch.bfloat16, device="cuda"), 1e-6)
+    assert e.value.status == ar.AR_ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("dtype,R,T,H,has_bias", [("bf16", 8, 40, 8192, True), ("fp16", 2, 9, 4096, True),
+                                                  ("fp32", 2, 4, 64, False)])
+def test_unfused_route_matches_oracle_composition(dtype, R, T, H, has_bias):
+    """ar_sum, then ar_residual_rmsnorm with the rounded sum as its one partial: the oracle composed the same way."""
+    inp = workloads.fused_inputs(R, T, H, dtype, partial_dist=("N", 0.0, 1.0 / R), residual_dist=("N", 0.0, 4.0),
+                                 bias_dist=("N", 0.0, 0.02) if has_bias else None, weight_dist=("N", 1.0, 0.05),
+                                 eps=1e-6, seed=T)
+    s = ar.ar_sum([dev(p) for p in inp.partials])
+    out, res = ar.ar_residual_rmsnorm([s], dev(inp.residual), dev(inp.weight), inp.eps, bias=dev(inp.bias))
+    torch.cuda.synchronize()
+    s_ref = oracle.sum(inp.partials, dtype)
+    tol.check_sum(s.cpu(), s_ref, [p.reshape(T, H) for p in inp.partials], dtype, "sum")
+    step2 = workloads.FusedInputs(1, T, H, dtype, inp.eps, [s_ref.reshape(T, H)], inp.residual, inp.weight, inp.bias)
+    check_fused(step2, out.cpu(), res.cpu())
