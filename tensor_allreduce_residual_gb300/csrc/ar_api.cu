@@ -145,6 +145,28 @@ int rule_vpt(int units_row, int tokens, int lanes, bool packed)
     return vpt;
 }
 
+// Rule for many rows when the measured table has no entry: the bulk-copy-fed
+// persistent kernel with at most 512 consumer threads per row (the fewest
+// chunks per row that allow it) and a ring of about kTmaRuleInflight bytes,
+// the depth that measured fastest on the 8192 x 8192 prefill.  False when
+// the row does not fit that kernel.
+constexpr int kTmaRuleMinTokens = 2048;
+constexpr int kTwoShotRuleMinTokens = 1024;
+constexpr size_t kTmaRuleInflight = 144 * 1024;
+
+bool tma_rule_shape(int units_row, int R, OneShotShape* sh)
+{
+    int cpr = 1;
+    while (cpr < 8 && (units_row + cpr - 1) / cpr > ar::tma_max_consumers(cpr))
+        cpr <<= 1;
+    const int nc = ((units_row + cpr - 1) / cpr + 31) / 32 * 32;
+    const size_t stage = static_cast<size_t>(R + 1) * nc * 16;
+    int stages = static_cast<int>((kTmaRuleInflight + stage / 2) / stage);
+    if (stages < ar::kTmaMinStages)
+        stages = ar::kTmaMinStages;
+    return tma_shape(units_row, cpr, R + 1, 1, stages, sh);
+}
+
 const ar::AutoEntry* table_lookup(int esize, int R, int units_row, int tokens)
 {
     for (const ar::AutoEntry& e : ar::kAutoTable) {
@@ -227,6 +249,18 @@ FusedPlan plan_fused(int esize, int R, int hidden, int tokens, bool packed, int 
             max_stages = ov.max_stages;
         }
     }
+    const bool measured = packed && (table_lookup(esize, R, units_row, tokens) != nullptr || shape_override().vpt > 0);
+    if (!measured && packed && tokens >= kTmaRuleMinTokens && tma_rule_shape(units_row, R, &p.shape)) {
+        p.shape.early_residual = 1;
+        p.oneshot_ok = true;
+        p.strategy = strategy == AR_AUTO ? AR_ONESHOT : strategy;
+        return p;
+    }
+    // Rows too long for the bulk-copy-fed kernel, many of them: the two-shot
+    // path (measured on 16384-wide bf16 rows: 29.7 us against 36.0 us for
+    // the register-resident one-shot kernel at 1024 rows).
+    if (!measured && tokens >= kTwoShotRuleMinTokens && units_row > ar::tma_max_consumers(8) * 8)
+        auto_strategy = AR_TWOSHOT;
     p.oneshot_ok = oneshot_shape(units_row, vpt, lanes, packed, mode, R, &p.shape, bps, max_stages);
     if (!p.oneshot_ok)  // the chosen shape does not fit this row: the rule's shape
         p.oneshot_ok = oneshot_shape(units_row, rule_vpt(units_row, tokens, lanes, packed), lanes,
@@ -247,8 +281,16 @@ int twoshot_nchunk(int units_row)
 
 size_t round256(size_t b) { return (b + 255) / 256 * 256; }
 
-// ar_rmsnorm takes the bulk-copy-fed kernel from this many rows on.
+// ar_rmsnorm takes the bulk-copy-fed kernel from this many rows on, for rows
+// of at most kNormTmaMaxUnits vectors, with this many chunks per row, blocks
+// per SM and ring slots per block.  Measured on 8192-row tensors: 8 KB rows
+// take 27.8 us this way against 37.7 us in the register-resident kernel;
+// 16 KB rows are faster in the register-resident kernel (76 us against 80).
 constexpr int kNormTmaMinTokens = 1024;
+constexpr int kNormTmaMaxUnits = 512;
+constexpr int kNormTmaVpt = 4;
+constexpr int kNormTmaBlocksPerSM = 4;
+constexpr int kNormTmaStages = 8;
 
 }  // namespace
 
@@ -423,14 +465,24 @@ int ar_rmsnorm(const void* x, const void* weight, float eps, int hidden, int tok
     const bool packed = hidden % lanes == 0 && aligned16(x) && aligned16(weight) && aligned16(out);
     const int units_row = packed ? hidden / lanes : hidden;
     OneShotShape sh{};
-    // Many rows: the bulk-copy-fed persistent kernel, about 128 KB of copies
-    // in flight per SM (x is the only streamed input).  Otherwise, and for
-    // rows it cannot hold, the register-resident row kernel.
-    bool tma = packed && tokens >= kNormTmaMinTokens &&
-               tma_shape(units_row, units_row <= 512 ? 1 : (units_row <= 1024 ? 2 : 4), 1, 1, 16, &sh);
-    if (!tma && !oneshot_shape(units_row, rule_vpt(units_row, tokens, packed ? lanes : 1, packed),
-                               packed ? lanes : 1, packed, ar::kRegisters, 1, &sh))
-        return AR_ERR_UNSUPPORTED;
+    // Many rows: the bulk-copy-fed persistent kernel (x is its only streamed
+    // input).  Otherwise, and for rows it cannot hold, the register-resident
+    // row kernel.  The shape override (measurement only) replaces both.
+    const ShapeOverride& ov = shape_override();
+    bool tma = false;
+    bool ok = false;
+    if (packed && ov.vpt > 0) {
+        tma = ov.mode == ar::kTma;
+        ok = tma ? tma_shape(units_row, ov.vpt, 1, ov.blocks_per_sm, ov.max_stages, &sh)
+                 : oneshot_shape(units_row, ov.vpt, lanes, packed, ar::kRegisters, 1, &sh);
+    }
+    if (!ok) {
+        tma = packed && tokens >= kNormTmaMinTokens && units_row <= kNormTmaMaxUnits &&
+              tma_shape(units_row, kNormTmaVpt, 1, kNormTmaBlocksPerSM, kNormTmaStages, &sh);
+        if (!tma && !oneshot_shape(units_row, rule_vpt(units_row, tokens, packed ? lanes : 1, packed),
+                                   packed ? lanes : 1, packed, ar::kRegisters, 1, &sh))
+            return AR_ERR_UNSUPPORTED;
+    }
     FusedArgs a{};
     a.partials[0] = x;
     a.weight = weight;
