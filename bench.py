@@ -386,6 +386,19 @@ def run_extras(ar, torch, workloads, parts, resid, weight, bias, out, res_out, w
         "us_per_call": round(ms * 1e3, 2), "GBps_effective": round(bytes_call / ms / 1e6, 1),
         "bytes_moved": moved, "GBps_moved": round(moved / ms / 1e6, 1),
         "fused_speedup": round(ms * 1e3 / ex["prefill_ONESHOT"]["us_per_call"], 3)}
+    # USE_MEMCPY (AllReduceStrategyConfig): the partials are first copied into
+    # the registered workspace, then reduced from there -- the cost of staging.
+    ws_cfg = torch.empty(ar.ar_config_workspace_size(len(parts), T_ * H_, H_, ar.AR_BF16), dtype=torch.uint8,
+                         device=resid.device)
+    prm = ar.make_params(parts, out, bias=bias, residual=resid, weight=weight, eps=EPS, hidden=H_,
+                         residual_out=res_out, workspace=ws_cfg)
+    ms = _time_calls(torch, lambda: ar.ar_allreduce_config(prm, ar.AR_FUSION_NONE, "AUTO",
+                                                           ar.AR_CONFIG_USE_MEMCPY | ar.AR_CONFIG_RESIDUAL_RMS_NORM),
+                     stream, 30)
+    ex["prefill_use_memcpy"] = {"us_per_call": round(ms * 1e3, 2), "GBps_effective": round(bytes_call / ms / 1e6, 1),
+                                "copy_bytes": 2 * len(parts) * T_ * H_ * 2,
+                                "staging_cost_vs_in_place": round(ms * 1e3 / ex["prefill_ONESHOT"]["us_per_call"], 3)}
+    del ws_cfg, prm
     ms = _time_calls(torch, lambda: ar.ar_rmsnorm(res_out, weight, EPS, out=out), stream, 50)
     nb = 2 * T_ * H_ * 2 + H_ * 2
     ex["prefill_rmsnorm_alone"] = {"us_per_call": round(ms * 1e3, 2), "bytes": nb, "GBps": round(nb / ms / 1e6, 1)}

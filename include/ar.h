@@ -261,6 +261,38 @@ typedef struct {
  * hidden).  Same errors as those two; AR_ERR_INVALID_ARG for a NULL p. */
 int ar_allreduce(const ar_params* p, int fusion_op, int strategy, ar_stream_t stream);
 
+/* AllReduceStrategyConfig bit flags ("type.d2"). */
+enum { AR_CONFIG_USE_MEMCPY = 1, AR_CONFIG_RESIDUAL_RMS_NORM = 2 };
+
+/*
+ * ar_config_workspace_size -- workspace bytes ar_allreduce_config needs with
+ * AR_CONFIG_USE_MEMCPY for R partials of n elements (hidden > 0 for the
+ * fused op, whose two-shot sums of squares follow the copies; 0 for the
+ * sum): R slots of n elements, each rounded up to 256 bytes, plus the
+ * fused workspace.  0 for an invalid shape.
+ */
+size_t ar_config_workspace_size(int R, size_t n, int hidden, int dtype);
+
+/*
+ * ar_allreduce_config -- ar_allreduce with the AllReduceStrategyConfig flags
+ * of "type.d2" (the `config` of AllReduceDispatchMemcpy in "allreduce.d2").
+ *   AR_CONFIG_RESIDUAL_RMS_NORM  run the fused op whatever fusion_op says.
+ *   AR_CONFIG_USE_MEMCPY         first copy every partials[r] (device to
+ *       device, on `stream`) into slot r of p->workspace, the caller's
+ *       registered buffer, and reduce from the copies; the fused op's
+ *       two-shot workspace follows the R slots.  p->workspace must be
+ *       256-byte aligned and hold ar_config_workspace_size(...) bytes.
+ *       On one GPU this only adds the copies' traffic: it measures what
+ *       staging the inputs costs against reading them in place.
+ * Results are bit-identical to ar_allreduce's.
+ * Errors: those of ar_allreduce, AR_ERR_UNSUPPORTED for unknown config
+ *         bits, AR_ERR_WORKSPACE for a missing, misaligned or small
+ *         workspace with AR_CONFIG_USE_MEMCPY, AR_ERR_CUDA if a copy cannot
+ *         be queued.  Argument errors of the reduction itself are found
+ *         after the copies are queued.
+ */
+int ar_allreduce_config(const ar_params* p, int fusion_op, int strategy, int config, ar_stream_t stream);
+
 /*
  * ar_query_strategy -- what AR_AUTO resolves to (the selectImplementation /
  * kernelLaunchConfig / heuristic_min_warp_number analogue, "allreduce.d2").

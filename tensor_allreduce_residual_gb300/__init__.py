@@ -29,6 +29,8 @@ AR_FUSION_NONE, AR_FUSION_RESIDUAL_RMS_NORM = 0, 1
 # status codes
 AR_OK, AR_ERR_INVALID_ARG, AR_ERR_UNSUPPORTED, AR_ERR_WORKSPACE, AR_ERR_CUDA, AR_ERR_TIMEOUT = 0, -1, -2, -3, -4, -5
 AR_MAX_RANKS = 16
+# AllReduceStrategyConfig bit flags
+AR_CONFIG_USE_MEMCPY, AR_CONFIG_RESIDUAL_RMS_NORM = 1, 2
 AR_NOALLOC_SCRATCH_BYTES = 1 << 20
 
 STRATEGIES = {"NCCL": AR_NCCL, "ONESHOT": AR_ONESHOT, "TWOSHOT": AR_TWOSHOT, "AUTO": AR_AUTO}
@@ -102,6 +104,9 @@ def lib() -> ctypes.CDLL:
     L.ar_device_status.argtypes, L.ar_device_status.restype = [], i
     L.ar_rmsnorm.argtypes, L.ar_rmsnorm.restype = [vp, vp, ctypes.c_float, i, i, vp, i, vp], i
     L.ar_host_staging_size.argtypes, L.ar_host_staging_size.restype = [i, i, i, i], sz
+    L.ar_config_workspace_size.argtypes, L.ar_config_workspace_size.restype = [i, sz, i, i], sz
+    L.ar_allreduce_config.argtypes = [ctypes.POINTER(ArParams), i, i, i, vp]
+    L.ar_allreduce_config.restype = i
     L.ar_residual_rmsnorm_host.argtypes = [pvp, i, vp, vp, vp, ctypes.c_float, i, i, vp, vp, vp, sz, i, i, i, vp]
     L.ar_residual_rmsnorm_host.restype = i
     L.ar_query_launch.argtypes = [i, i, i, i, i, ctypes.POINTER(ArLaunchPlan)]
@@ -337,6 +342,17 @@ def ar_allreduce(params: ArParams, fusion_op: int, strategy="AUTO", stream=None)
     """Calls ar_allreduce with a filled ArParams structure (raw device pointers)."""
     _check("ar_allreduce", lib().ar_allreduce(ctypes.byref(params), fusion_op, _strategy(strategy),
                                               _stream_handle(stream)))
+
+
+def ar_config_workspace_size(R: int, n: int, hidden: int, dtype) -> int:
+    code = dtype if isinstance(dtype, int) else dtype_code(dtype)
+    return int(lib().ar_config_workspace_size(R, n, hidden, code))
+
+
+def ar_allreduce_config(params: ArParams, fusion_op: int, strategy="AUTO", config: int = 0, stream=None) -> None:
+    """Calls ar_allreduce_config (AllReduceStrategyConfig flags in `config`) with a filled ArParams."""
+    _check("ar_allreduce_config", lib().ar_allreduce_config(ctypes.byref(params), fusion_op, _strategy(strategy),
+                                                            config, _stream_handle(stream)))
 
 
 def make_params(partials, out, *, bias=None, residual=None, weight=None, eps=0.0, hidden=0,

@@ -591,6 +591,66 @@ int ar_device_status(void)
     return total != 0 ? AR_ERR_TIMEOUT : AR_OK;
 }
 
+size_t ar_config_workspace_size(int R, size_t n, int hidden, int dtype)
+{
+    const int esize = esize_of(dtype);
+    if (R < 1 || R > AR_MAX_RANKS || n == 0 || esize == 0 || hidden < 0)
+        return 0;
+    size_t fused = 0;
+    if (hidden > 0) {
+        if (n % static_cast<size_t>(hidden) != 0 || n / static_cast<size_t>(hidden) > static_cast<size_t>(INT32_MAX))
+            return 0;
+        fused = ar_workspace_size_rows(R, hidden, static_cast<int>(n / static_cast<size_t>(hidden)), dtype);
+    }
+    return static_cast<size_t>(R) * round256(n * esize) + fused;
+}
+
+int ar_allreduce_config(const ar_params* p, int fusion_op, int strategy, int config, ar_stream_t stream)
+{
+    if (p == nullptr)
+        return AR_ERR_INVALID_ARG;
+    if ((config & ~(AR_CONFIG_USE_MEMCPY | AR_CONFIG_RESIDUAL_RMS_NORM)) != 0)
+        return AR_ERR_UNSUPPORTED;
+    const int op = (config & AR_CONFIG_RESIDUAL_RMS_NORM) ? AR_FUSION_RESIDUAL_RMS_NORM : fusion_op;
+    if (!(config & AR_CONFIG_USE_MEMCPY))
+        return ar_allreduce(p, op, strategy, stream);
+    if (op != AR_FUSION_NONE && op != AR_FUSION_RESIDUAL_RMS_NORM)
+        return AR_ERR_UNSUPPORTED;
+    if (p->R < 1 || p->R > AR_MAX_RANKS)
+        return AR_ERR_INVALID_ARG;
+    const int esize = esize_of(p->dtype);
+    if (esize == 0)
+        return AR_ERR_UNSUPPORTED;
+    if (p->n == 0)
+        return ar_allreduce(p, op, strategy, stream);
+    for (int r = 0; r < p->R; ++r)
+        if (p->partials[r] == nullptr)
+            return AR_ERR_INVALID_ARG;
+    const int hidden = op == AR_FUSION_RESIDUAL_RMS_NORM ? p->hidden : 0;
+    if (op == AR_FUSION_RESIDUAL_RMS_NORM && (p->hidden < 1 || p->n % static_cast<size_t>(p->hidden) != 0))
+        return AR_ERR_INVALID_ARG;
+    const size_t need = ar_config_workspace_size(p->R, p->n, hidden, p->dtype);
+    if (need == 0)
+        return AR_ERR_INVALID_ARG;
+    if (p->workspace == nullptr || p->workspace_bytes < need ||
+        (reinterpret_cast<uintptr_t>(p->workspace) & 255u) != 0)
+        return AR_ERR_WORKSPACE;
+    // Stage every partial into its slot of the registered buffer, then reduce
+    // from the slots (the USE_MEMCPY route of AllReduceDispatchMemcpy).
+    const size_t slot = round256(p->n * esize);
+    char* ws = static_cast<char*>(p->workspace);
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    ar_params q = *p;
+    for (int r = 0; r < p->R; ++r) {
+        if (cudaMemcpyAsync(ws + r * slot, p->partials[r], p->n * esize, cudaMemcpyDeviceToDevice, s) != cudaSuccess)
+            return AR_ERR_CUDA;
+        q.partials[r] = ws + r * slot;
+    }
+    q.workspace = ws + static_cast<size_t>(p->R) * slot;
+    q.workspace_bytes = p->workspace_bytes - static_cast<size_t>(p->R) * slot;
+    return ar_allreduce(&q, op, strategy, stream);
+}
+
 int ar_query_strategy(int R, size_t n, int hidden, int dtype, int fusion_op, int* chosen,
                       int* warps_per_token)
 {

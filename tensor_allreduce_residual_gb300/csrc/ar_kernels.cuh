@@ -26,6 +26,22 @@
 namespace ar {
 
 // ---------------------------------------------------------------------------
+// Programmatic dependent launch (sm_90 and later).  Kernels here are launched
+// with the programmatic-stream-serialization attribute, so one may start
+// (get its blocks resident, set up shared memory) while the previous kernel
+// in its stream is still running.  griddepcontrol.wait then blocks until
+// every prerequisite grid has completed and its memory is visible, so each
+// kernel calls pdl_enter() before it touches any global buffer, input or
+// output.  It then lets the next kernel in the stream launch early too.
+// Without the attribute both instructions do nothing.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void pdl_enter()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// ---------------------------------------------------------------------------
 // 16-byte packed vectors and single elements.
 // ---------------------------------------------------------------------------
 
@@ -220,6 +236,7 @@ template <typename T, bool PACKED, int R_CT, int UNROLL>
 __global__ void __launch_bounds__(kFlatThreads)
 k_sum(const SumArgs a)
 {
+    pdl_enter();
     using U = Unit<T, PACKED>;
     constexpr int L = U::L;
     const uint64_t s_begin = static_cast<uint64_t>(blockIdx.y) * a.slice;
@@ -350,6 +367,7 @@ template <typename T, bool PACKED, int R_CT, int VPT, bool STAGE, bool EARLY>
 __global__ void __launch_bounds__(STAGE ? 1024 : oneshot_max_threads(VPT * Unit<T, PACKED>::L))
 k_fused_oneshot(const FusedArgs a, const int tpr)
 {
+    pdl_enter();
     using U = Unit<T, PACKED>;
     constexpr int L = U::L;
     __shared__ float red[32];
@@ -437,6 +455,7 @@ template <typename T, int R_CT, int VPT>
 __global__ void __launch_bounds__(kMaxPersistThreads)
 k_fused_oneshot_persist(const FusedArgs a)
 {
+    pdl_enter();
     using U = Unit<T, true>;
     constexpr int L = U::L;
     static_assert(R_CT > 0, "persistent one-shot needs R at compile time");
@@ -532,6 +551,7 @@ template <typename T, bool PACKED, int VPT>
 __global__ void __launch_bounds__(oneshot_max_threads(VPT * Unit<T, PACKED>::L))
 k_rmsnorm(const FusedArgs a, const int tpr)
 {
+    pdl_enter();
     using U = Unit<T, PACKED>;
     constexpr int L = U::L;
     __shared__ float red[32];
@@ -585,6 +605,7 @@ template <typename T, bool PACKED, int R_CT>
 __global__ void __launch_bounds__(kFlatThreads)
 k_twoshot_phase1(const FusedArgs a)
 {
+    pdl_enter();
     using U = Unit<T, PACKED>;
     constexpr int L = U::L;
     __shared__ float red[kFlatThreads / 32];
@@ -630,6 +651,7 @@ template <typename T, bool PACKED>
 __global__ void __launch_bounds__(kFlatThreads)
 k_twoshot_phase2(const FusedArgs a)
 {
+    pdl_enter();
     using U = Unit<T, PACKED>;
     constexpr int L = U::L;
 

@@ -10,11 +10,43 @@
 #pragma once
 
 #include <climits>
+#include <cstdlib>
+#include <utility>
 
 #include "ar_kernels.cuh"
 #include "ar_tma.cuh"
 
 namespace ar {
+
+// Programmatic dependent launch is on unless AR_PDL=0 (read once; kept for
+// measuring its effect).
+inline bool pdl_enabled()
+{
+    static const bool on = [] {
+        const char* e = std::getenv("AR_PDL");
+        return !(e != nullptr && e[0] == '0');
+    }();
+    return on;
+}
+
+// Launches `kernel` on `s` with the programmatic-stream-serialization
+// attribute (see pdl_enter in ar_kernels.cuh); returns the launch status.
+template <typename... KArgs, typename... Args>
+static cudaError_t launch_k(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                            Args&&... args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl_enabled() ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 template <typename T, bool PACKED, int R_CT, int UNROLL>
 static cudaError_t run_sum(const SumArgs& a, int nslices, cudaStream_t s)
@@ -26,8 +58,7 @@ static cudaError_t run_sum(const SumArgs& a, int nslices, cudaStream_t s)
     if (gx > static_cast<uint64_t>(INT_MAX))
         return cudaErrorInvalidConfiguration;
     dim3 grid(static_cast<unsigned>(gx), static_cast<unsigned>(nslices));
-    k_sum<T, PACKED, R_CT, UNROLL><<<grid, kFlatThreads, 0, s>>>(a);
-    return cudaGetLastError();
+    return launch_k(k_sum<T, PACKED, R_CT, UNROLL>, grid, dim3(kFlatThreads), 0, s, a);
 }
 
 template <typename T>
@@ -61,8 +92,7 @@ static cudaError_t run_oneshot(const FusedArgs& a, OneShotShape sh, cudaStream_t
     }
     const int threads = sh.tpr * sh.rows;
     const unsigned grid = static_cast<unsigned>((a.tokens + sh.rows - 1) / sh.rows);
-    kernel<<<grid, threads, STAGE ? sh.smem_bytes : 0, s>>>(a, sh.tpr);
-    return cudaGetLastError();
+    return launch_k(kernel, dim3(grid), dim3(threads), STAGE ? sh.smem_bytes : 0, s, a, sh.tpr);
 }
 
 template <typename T, bool PACKED, int R_CT, bool STAGE, bool EARLY>
@@ -108,8 +138,7 @@ static cudaError_t run_persist(const FusedArgs& a, OneShotShape sh, cudaStream_t
         return e;
     const long long resident = static_cast<long long>(sms) * (per_sm > 0 ? per_sm : 1);
     const unsigned grid = static_cast<unsigned>(a.tokens < resident ? a.tokens : resident);
-    kernel<<<grid, sh.tpr, sh.smem_bytes, s>>>(a);
-    return cudaGetLastError();
+    return launch_k(kernel, dim3(grid), dim3(sh.tpr), sh.smem_bytes, s, a);
 }
 
 // Persistent blocks fed by bulk copies: sh.tpr consumer threads plus one
@@ -130,8 +159,7 @@ static cudaError_t run_tma(const FusedArgs& a, OneShotShape sh, cudaStream_t s)
         return e;
     const long long slots = static_cast<long long>(sms) * sh.blocks_per_sm;
     const unsigned grid = static_cast<unsigned>(a.tokens < slots ? a.tokens : slots);
-    kernel<<<grid, sh.tpr + 32, sh.smem_bytes, s>>>(a, sh.stages);
-    return cudaGetLastError();
+    return launch_k(kernel, dim3(grid), dim3(sh.tpr + 32), sh.smem_bytes, s, a, sh.stages);
 }
 
 template <typename T, int R_CT>
@@ -179,8 +207,7 @@ template <typename T, bool PACKED, int VPT>
 static cudaError_t run_rmsnorm(const FusedArgs& a, OneShotShape sh, cudaStream_t s)
 {
     const unsigned grid = static_cast<unsigned>((a.tokens + sh.rows - 1) / sh.rows);
-    k_rmsnorm<T, PACKED, VPT><<<grid, sh.tpr * sh.rows, 0, s>>>(a, sh.tpr);
-    return cudaGetLastError();
+    return launch_k(k_rmsnorm<T, PACKED, VPT>, dim3(grid), dim3(sh.tpr * sh.rows), 0, s, a, sh.tpr);
 }
 
 template <typename T, bool PACKED>
@@ -223,12 +250,11 @@ static cudaError_t run_twoshot(const FusedArgs& a, cudaStream_t s)
     const uint64_t blocks = static_cast<uint64_t>(a.tokens) * a.nchunk;
     if (blocks > static_cast<uint64_t>(INT_MAX))
         return cudaErrorInvalidConfiguration;
-    k_twoshot_phase1<T, PACKED, R_CT><<<static_cast<unsigned>(blocks), kFlatThreads, 0, s>>>(a);
-    cudaError_t e = cudaGetLastError();
+    const cudaError_t e = launch_k(k_twoshot_phase1<T, PACKED, R_CT>, dim3(static_cast<unsigned>(blocks)),
+                                   dim3(kFlatThreads), 0, s, a);
     if (e != cudaSuccess)
         return e;
-    k_twoshot_phase2<T, PACKED><<<static_cast<unsigned>(blocks), kFlatThreads, 0, s>>>(a);
-    return cudaGetLastError();
+    return launch_k(k_twoshot_phase2<T, PACKED>, dim3(static_cast<unsigned>(blocks)), dim3(kFlatThreads), 0, s, a);
 }
 
 template <typename T>

@@ -153,6 +153,7 @@ k_fused_oneshot_tma(const FusedArgs a, const int stages)
         fence_mbar_init();
     }
     __syncthreads();
+    pdl_enter();  // shared-memory set-up above overlaps the previous kernel
 
     if (tid >= nc) {
         // Producer warp: one lane issues every copy.

@@ -38,7 +38,8 @@ def test_header_declares_the_expected_entry_points():
     names = _declared_functions()
     for want in ["ar_version", "ar_strerror", "ar_workspace_size", "ar_workspace_size_rows", "ar_sum",
                  "ar_residual_rmsnorm", "ar_allreduce", "ar_query_strategy", "ar_query_launch", "ar_device_status",
-                 "ar_rmsnorm", "ar_host_staging_size", "ar_residual_rmsnorm_host"]:
+                 "ar_rmsnorm", "ar_host_staging_size", "ar_residual_rmsnorm_host", "ar_config_workspace_size",
+                 "ar_allreduce_config"]:
         assert want in names, names
 
 
@@ -287,3 +288,24 @@ def test_host_staging_size_and_errors(L):
     assert call(nbytes=100) == ar.AR_ERR_WORKSPACE
     assert call(staging=FAKE + 16) == ar.AR_ERR_WORKSPACE        # not 256-byte aligned
     assert call(T=0) == ar.AR_OK
+
+
+def test_allreduce_config_errors_and_sizes(L):
+    assert L.ar_config_workspace_size(4, 1000, 0, ar.AR_FP16) == 4 * 2048          # 2000 B -> 2048 per slot
+    assert L.ar_config_workspace_size(2, 64 * 4, 64, ar.AR_FP32) == 2 * 1024 + L.ar_workspace_size_rows(2, 64, 4, ar.AR_FP32)
+    assert L.ar_config_workspace_size(0, 100, 0, ar.AR_FP16) == 0
+    assert L.ar_config_workspace_size(2, 100, 64, ar.AR_FP16) == 0                 # not a whole number of rows
+    assert L.ar_allreduce_config(None, 0, ar.AR_ONESHOT, 1, None) == ar.AR_ERR_INVALID_ARG
+    p = ar.ArParams()
+    p.R, p.dtype, p.n = 2, ar.AR_FP16, 1024
+    p.partials[0], p.partials[1], p.out = FAKE, FAKE + 4096, FAKE + 8192
+    assert L.ar_allreduce_config(ctypes.byref(p), 0, ar.AR_ONESHOT, 4, None) == ar.AR_ERR_UNSUPPORTED
+    assert L.ar_allreduce_config(ctypes.byref(p), 0, ar.AR_ONESHOT, 1, None) == ar.AR_ERR_WORKSPACE   # no workspace
+    p.workspace, p.workspace_bytes = FAKE + 16, 1 << 20
+    assert L.ar_allreduce_config(ctypes.byref(p), 0, ar.AR_ONESHOT, 1, None) == ar.AR_ERR_WORKSPACE   # misaligned
+    p.workspace, p.workspace_bytes = FAKE, 100
+    assert L.ar_allreduce_config(ctypes.byref(p), 0, ar.AR_ONESHOT, 1, None) == ar.AR_ERR_WORKSPACE   # too small
+    p.partials[1] = None
+    assert L.ar_allreduce_config(ctypes.byref(p), 0, ar.AR_ONESHOT, 1, None) == ar.AR_ERR_INVALID_ARG
+    p.n = 0
+    assert L.ar_allreduce_config(ctypes.byref(p), 0, ar.AR_ONESHOT, 1, None) == ar.AR_OK

@@ -412,3 +412,36 @@ def test_unfused_route_matches_oracle_composition(dtype, R, T, H, has_bias):
     tol.check_sum(s.cpu(), s_ref, [p.reshape(T, H) for p in inp.partials], dtype, "sum")
     step2 = workloads.FusedInputs(1, T, H, dtype, inp.eps, [s_ref.reshape(T, H)], inp.residual, inp.weight, inp.bias)
     check_fused(step2, out.cpu(), res.cpu())
+
+
+@pytest.mark.parametrize("config", [ar.AR_CONFIG_USE_MEMCPY, ar.AR_CONFIG_RESIDUAL_RMS_NORM,
+                                    ar.AR_CONFIG_USE_MEMCPY | ar.AR_CONFIG_RESIDUAL_RMS_NORM])
+@pytest.mark.parametrize("strategy", ["ONESHOT", "TWOSHOT"])
+def test_allreduce_config_flags_match_allreduce(config, strategy):
+    """USE_MEMCPY (stage the partials in the registered workspace first) and the RESIDUAL_RMS_NORM
+    flag give the same bits as ar_allreduce with the matching fusion op."""
+    f = workloads.fused_inputs(8, 33, 8192, "bf16", partial_dist=("N", 0.0, 0.125), residual_dist=("N", 0.0, 4.0),
+                               bias_dist=("N", 0.0, 0.02), weight_dist=("N", 1.0, 0.05), eps=1e-6, seed=config)
+    parts = [dev(p) for p in f.partials]
+    fused = bool(config & ar.AR_CONFIG_RESIDUAL_RMS_NORM)
+    outs = []
+    for cfg in (None, config):
+        out, rout = torch.empty_like(parts[0]), torch.empty_like(parts[0])
+        ws = torch.empty(ar.ar_config_workspace_size(8, out.numel(), 8192, ar.AR_BF16), dtype=torch.uint8,
+                         device="cuda")
+        p = ar.make_params(parts, out, bias=dev(f.bias), residual=dev(f.residual), weight=dev(f.weight), eps=f.eps,
+                           hidden=8192, residual_out=rout, workspace=ws)
+        op = ar.AR_FUSION_RESIDUAL_RMS_NORM if fused else ar.AR_FUSION_NONE
+        if cfg is None:
+            ar.ar_allreduce(p, op, strategy)
+        else:
+            ar.ar_allreduce_config(p, ar.AR_FUSION_NONE, strategy, cfg)
+        torch.cuda.synchronize()
+        outs.append((out.cpu(), rout.cpu() if fused else None))
+    assert torch.equal(outs[0][0].view(torch.int16), outs[1][0].view(torch.int16))
+    if fused:
+        assert torch.equal(outs[0][1].view(torch.int16), outs[1][1].view(torch.int16))
+    if fused:
+        check_fused(f, *outs[1])
+    else:
+        tol.check_sum(outs[1][0], oracle.sum(f.partials, "bf16"), [q.reshape(33, 8192) for q in f.partials], "bf16")
