@@ -281,16 +281,34 @@ int twoshot_nchunk(int units_row)
 
 size_t round256(size_t b) { return (b + 255) / 256 * 256; }
 
-// ar_rmsnorm takes the bulk-copy-fed kernel from this many rows on, for rows
-// of at most kNormTmaMaxUnits vectors, with this many chunks per row, blocks
-// per SM and ring slots per block.  Measured on 8192-row tensors: 8 KB rows
-// take 27.8 us this way against 37.7 us in the register-resident kernel;
-// 16 KB rows are faster in the register-resident kernel (76 us against 80).
-constexpr int kNormTmaMinTokens = 1024;
-constexpr int kNormTmaMaxUnits = 512;
-constexpr int kNormTmaVpt = 4;
-constexpr int kNormTmaBlocksPerSM = 4;
-constexpr int kNormTmaStages = 8;
+// Register-resident norm shape: 4 packed vectors per thread for rows of
+// 1024 vectors or more, 8 below (16 elements on the element-wise path), and
+// fewer when a row would get less than a warp; blocks of at least 128
+// threads.  Measured on 8192-row tensors: 46.6 us (8192 bf16, 4 per thread)
+// and 20.8 us (4096 fp16, 8 per thread), 0.85 and 0.95 of the copy peak.
+// `vpt` forces the units per thread (measurement only).  False when the row
+// does not fit one block.
+bool norm_shape(int units_row, bool packed, OneShotShape* sh, int vpt = 0)
+{
+    const int max_vpt = packed ? ar::kMaxVPTVec : ar::kMaxVPTScalar;
+    if (vpt <= 0) {
+        vpt = packed && units_row >= 1024 ? 4 : max_vpt;
+        while (vpt > 1 && (units_row + vpt - 1) / vpt < 32)
+            vpt >>= 1;
+    }
+    if (vpt > max_vpt)
+        return false;
+    const int tpr = next_pow2((units_row + vpt - 1) / vpt);
+    if (tpr > ar::norm_max_threads(packed, vpt))
+        return false;
+    sh->tpr = tpr;
+    sh->vpt = vpt;
+    sh->rows = tpr >= 128 ? 1 : 128 / tpr;
+    sh->mode = ar::kRegisters;
+    sh->smem_bytes = 0;
+    return true;
+}
+
 
 }  // namespace
 
@@ -465,22 +483,21 @@ int ar_rmsnorm(const void* x, const void* weight, float eps, int hidden, int tok
     const bool packed = hidden % lanes == 0 && aligned16(x) && aligned16(weight) && aligned16(out);
     const int units_row = packed ? hidden / lanes : hidden;
     OneShotShape sh{};
-    // Many rows: the bulk-copy-fed persistent kernel (x is its only streamed
-    // input).  Otherwise, and for rows it cannot hold, the register-resident
-    // row kernel.  The shape override (measurement only) replaces both.
+    // The register-resident row kernel.  The shape override (measurement
+    // only) can force its units per thread, or the bulk-copy-fed persistent
+    // kernel with x as its only streamed input (slower here: 80 us at
+    // 8192 x 8192 bf16, 27 us at 8192 x 4096 fp16).
     const ShapeOverride& ov = shape_override();
     bool tma = false;
     bool ok = false;
     if (packed && ov.vpt > 0) {
         tma = ov.mode == ar::kTma;
         ok = tma ? tma_shape(units_row, ov.vpt, 1, ov.blocks_per_sm, ov.max_stages, &sh)
-                 : oneshot_shape(units_row, ov.vpt, lanes, packed, ar::kRegisters, 1, &sh);
+                 : norm_shape(units_row, packed, &sh, ov.vpt);
     }
     if (!ok) {
-        tma = packed && tokens >= kNormTmaMinTokens && units_row <= kNormTmaMaxUnits &&
-              tma_shape(units_row, kNormTmaVpt, 1, kNormTmaBlocksPerSM, kNormTmaStages, &sh);
-        if (!tma && !oneshot_shape(units_row, rule_vpt(units_row, tokens, packed ? lanes : 1, packed),
-                                   packed ? lanes : 1, packed, ar::kRegisters, 1, &sh))
+        tma = false;
+        if (!norm_shape(units_row, packed, &sh))
             return AR_ERR_UNSUPPORTED;
     }
     FusedArgs a{};

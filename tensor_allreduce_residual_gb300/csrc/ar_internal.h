@@ -38,6 +38,14 @@ __host__ __device__ constexpr int oneshot_max_threads(int values)
     return values <= 16 ? 1024 : (values <= 32 ? 512 : 256);
 }
 
+// Largest block of the norm kernel k_rmsnorm for `vpt` units per thread: 8
+// packed vectors (32 registers of row data) need a 512-thread cap to stay
+// out of local memory; everything else fits 1024 threads.
+__host__ __device__ constexpr int norm_max_threads(bool packed, int vpt)
+{
+    return packed && vpt >= 8 ? 512 : kMaxTPR;
+}
+
 struct SumArgs {
     const void* partials[kMaxRanks];
     void* out;

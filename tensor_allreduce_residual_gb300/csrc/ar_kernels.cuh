@@ -542,13 +542,18 @@ k_fused_oneshot_persist(const FusedArgs a)
 
 // ---------------------------------------------------------------------------
 // RMSNorm of x rows on its own (rms_norm_kernel_launcher -> rms_norm_kernel,
-// "allreduce.d2": the norm that follows a plain all-reduce).  Same layout
-// as the register-resident one-shot kernel: `tpr` threads own a row, each
-// keeps VPT units of x in registers across the row reduction, so x is read
-// once and out written once.  x is a.partials[0]; out may alias x.
+// "allreduce.d2": the norm that follows a plain all-reduce).  `tpr` threads
+// own a row and each keeps VPT units of it in registers across the row
+// reduction, so x is read from HBM once and out written once.  Unlike the
+// fused kernels, the row here is the input itself: the registers hold the
+// packed 16-byte vectors as loaded (half the registers of fp32 values for
+// 16-bit types) and the second pass unpacks them again, exactly; the weight
+// is loaded only in the second pass (it is small and cache-resident).  Fewer
+// registers per row mean more rows, and more bytes, in flight per SM.
+// x is a.partials[0]; out may alias x.
 // ---------------------------------------------------------------------------
 template <typename T, bool PACKED, int VPT>
-__global__ void __launch_bounds__(oneshot_max_threads(VPT * Unit<T, PACKED>::L))
+__global__ void __launch_bounds__(norm_max_threads(PACKED, VPT))
 k_rmsnorm(const FusedArgs a, const int tpr)
 {
     pdl_enter();
@@ -561,21 +566,23 @@ k_rmsnorm(const FusedArgs a, const int tpr)
     const bool row_ok = row < a.tokens;
     const uint64_t row_off = static_cast<uint64_t>(row) * a.units_row;
 
-    float x[VPT][L];
-    typename U::raw wv[VPT];
+    typename U::raw xr[VPT];
+#pragma unroll
+    for (int k = 0; k < VPT; ++k) {
+        const int j = lane_row + k * tpr;
+        if (row_ok && j < a.units_row)
+            xr[k] = U::load(a.partials[0], row_off + j);
+    }
     float ss = 0.0f;
 #pragma unroll
     for (int k = 0; k < VPT; ++k) {
         const int j = lane_row + k * tpr;
-#pragma unroll
-        for (int l = 0; l < L; ++l)
-            x[k][l] = 0.0f;
         if (row_ok && j < a.units_row) {
-            U::to_float(U::load(a.partials[0], row_off + j), x[k]);
-            wv[k] = U::load_cached(a.weight, j);
+            float x[L];
+            U::to_float(xr[k], x);
 #pragma unroll
             for (int l = 0; l < L; ++l)
-                ss = fmaf(x[k][l], x[k][l], ss);
+                ss = fmaf(x[l], x[l], ss);
         }
     }
     ss = row_sum(ss, tpr, red);
@@ -584,11 +591,12 @@ k_rmsnorm(const FusedArgs a, const int tpr)
     for (int k = 0; k < VPT; ++k) {
         const int j = lane_row + k * tpr;
         if (row_ok && j < a.units_row) {
-            float w[L], y[L];
-            U::to_float(wv[k], w);
+            float x[L], w[L], y[L];
+            U::to_float(xr[k], x);
+            U::to_float(U::load_cached(a.weight, j), w);
 #pragma unroll
             for (int l = 0; l < L; ++l)
-                y[l] = x[k][l] * inv * w[l];
+                y[l] = x[l] * inv * w[l];
             U::store(a.out, row_off + j, y);
         }
     }

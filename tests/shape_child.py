@@ -48,6 +48,16 @@ def main():
     # a rank count without a compile-time specialisation
     check(workloads.fused_inputs(3, 21, 4096, "fp16", partial_dist=("N", 0.0, 0.3), residual_dist=("N", 0.0, 4.0),
                                  bias_dist=("N", 0.0, 0.02), weight_dist=("N", 1.0, 0.05), eps=1e-5, seed=7))
+    # The norm on its own under the same shape: the register-resident kernel
+    # with these units per thread, or the bulk-copy-fed kernel streaming x alone.
+    for T, H, dt in [(37, 8192, "bf16"), (21, 8000, "bf16"), (9, 4096, "fp16"), (5, 1024, "fp32")]:
+        g = torch.Generator().manual_seed(T + H)
+        x = (torch.randn(T, H, generator=g, dtype=torch.float64) * 2).to(workloads.DTYPES[dt]).contiguous()
+        w = (1 + 0.05 * torch.randn(H, generator=g, dtype=torch.float64)).to(workloads.DTYPES[dt]).contiguous()
+        got = ar.ar_rmsnorm(x.cuda(), w.cuda(), 1e-6)
+        torch.cuda.synchronize()
+        ref, inv = oracle.rmsnorm(x, w, 1e-6, dt)
+        tol.check_fused_out(got.cpu(), ref, [x], w, inv, dt, H, f"rmsnorm {T}x{H} {dt}")
     assert ar.ar_device_status() == ar.AR_OK, "a kernel gave up a bounded wait"
     print("shape ok")
 

@@ -373,7 +373,7 @@ def _norm_rows(T, H, dtype, seed, scale=2.0):
 
 @pytest.mark.parametrize("dtype", ["fp32", "fp16", "bf16"])
 @pytest.mark.parametrize("T,H", [(1, 4096), (7, 8192), (300, 64), (33, 16384), (5, 100), (3, 3), (129, 1024),
-                                 # 1024 rows or more: the bulk-copy-fed kernel (ragged chunks at H=8000)
+                                 # 1024 rows or more, ragged rows (H=8000), and rows of under a warp (H=64)
                                  (1500, 8192), (1024, 8000), (1100, 1000), (1030, 64), (1024, 16384)])
 def test_rmsnorm_matches_oracle(dtype, T, H):
     x, w = _norm_rows(T, H, dtype, seed=T * 7 + H)
