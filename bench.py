@@ -38,7 +38,9 @@ R, TOKENS, HIDDEN, EPS = 8, 8192, 8192, 1e-6
 DATA = ("synthetic, seeded: partials N(0,1/8), residual N(0,4), bias N(0,0.02), weight N(1,0.05) "
         "(second argument = variance), drawn in fp32 and rounded to bf16")
 FALLBACK_HBM_GBS = 6800.0
-KERNEL_SOURCES = ["ar_kernels.cuh", "ar_tma.cuh", "ar_launch.cuh", "ar_internal.h", "ar_api.cu", "ar_auto_table.h"]
+# Device code whose DRAM counters a committed ncu summary records (the launch
+# shape is checked separately, through the launch plan).
+KERNEL_SOURCES = ["ar_kernels.cuh", "ar_tma.cuh", "ar_launch.cuh", "ar_internal.h"]
 
 
 def parse_args():
@@ -80,8 +82,15 @@ def measured_peaks():
     return FALLBACK_HBM_GBS, "of fallback"
 
 
-def profiled_traffic(kernel_tag: str):
-    """dram bytes per launch from a committed ncu summary, if it was taken on the current kernel sources."""
+def plan_key(plan: dict) -> str:
+    """The launch shape of a fused call, as recorded beside its ncu counters."""
+    return ":".join(str(plan[k]) for k in ("kernel_name", "threads_per_block", "units_per_thread", "stages",
+                                           "blocks_per_sm", "smem_bytes"))
+
+
+def profiled_traffic(kernel_tag: str, launch_plan: str):
+    """dram bytes per launch from a committed ncu summary, if it was taken on the current device code and
+    the same launch shape; None otherwise."""
     pdir = os.path.join(ROOT, "profiles")
     if not os.path.isdir(pdir):
         return None
@@ -92,8 +101,10 @@ def profiled_traffic(kernel_tag: str):
         text = open(os.path.join(pdir, name)).read()
         m_tag = re.search(r"^roofline_kernel:\s*(\S+)", text, re.M)
         m_hash = re.search(r"^kernel_sources_sha256:\s*(\S+)", text, re.M)
+        m_plan = re.search(r"^launch_plan:\s*(\S+)", text, re.M)
         m_tr = re.search(r"^traffic_bytes_per_launch:\s*([0-9.eE+]+)", text, re.M)
-        if m_tag and m_hash and m_tr and m_tag.group(1) == kernel_tag and m_hash.group(1) == want:
+        if (m_tag and m_hash and m_plan and m_tr and m_tag.group(1) == kernel_tag and m_hash.group(1) == want
+                and m_plan.group(1) == launch_plan):
             return float(m_tr.group(1))
     return None
 
@@ -238,7 +249,7 @@ def run_ours(args, rank, world, local_rank):
     mean_launch_ms = statistics.fmean(per_step)
     achieved = bytes_call / (mean_launch_ms * 1e-3) / 1e9
     kernel_tag = plan["kernel_name"]
-    traffic = profiled_traffic(kernel_tag)
+    traffic = profiled_traffic(kernel_tag, plan_key(plan))
     roofline = {"bound": "hbm", "kernel": kernel_tag, "achieved": round(achieved, 1), "peak": peak,
                 "unit": "GB/s", "frac": round(achieved / peak, 4), "peak_source": peak_src,
                 "traffic": traffic, "algorithmic_bytes_per_launch": bytes_call,
@@ -405,6 +416,22 @@ def run_extras(ar, torch, workloads, parts, resid, weight, bias, out, res_out, w
     del tmp
 
     flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    # PR1 reference case: R=2 fp32, 4 x 64, fusion NONE and RESIDUAL_RMS_NORM.
+    p1 = workloads.pr1(seed=0)
+    p1d = [t.cuda() for t in p1.partials]
+    p1r, p1w, p1b = p1.residual.cuda(), p1.weight.cuda(), p1.bias.cuda()
+    ex["pr1_R2_fp32_T4_H64"] = {
+        "fused_us_graph": round(_time_graph(torch, lambda: ar.ar_residual_rmsnorm(p1d, p1r, p1w, p1.eps, bias=p1b,
+                                                                                  strategy="AUTO")) * 1e3, 2),
+        "sum_us_graph": round(_time_graph(torch, lambda: ar.ar_sum(p1d, strategy="AUTO")) * 1e3, 2)}
+    dec_all = {}
+    for T in workloads.TP_DECODE_TOKENS:
+        f = workloads.tp_decode(T, device="cuda")
+        o, r = torch.empty_like(f.residual), torch.empty_like(f.residual)
+        dec_all[T] = round(_time_graph(torch, lambda f=f, o=o, r=r: ar.ar_residual_rmsnorm(
+            f.partials, f.residual, f.weight, f.eps, bias=f.bias, out=o, residual_out=r, strategy="ONESHOT"),
+            n=20, reps=3) * 1e3, 2)
+    ex["tp_decode_R2_fp16_H4096_us_graph_by_tokens"] = dec_all
     dec = {}
     for T in (1, 8, 32):
         f = workloads.tp_decode(T, device="cuda")

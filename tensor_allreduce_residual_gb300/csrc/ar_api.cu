@@ -65,10 +65,6 @@ int next_pow2(int v)
 
 // ---------------------------------------------------------------- one-shot shape
 
-// Threads per row = units_row / vpt rounded up to a power of two; blocks hold
-// at least 128 threads.  Register-resident rows are limited by the registers
-// a thread may use, staged rows by shared memory.  Returns false when the
-// row does not fit (then only the two-shot path can take it).
 // Bulk-copy-fed persistent shape (mode kTma): vpt = chunks per row, one
 // consumer thread per vector of a chunk (a multiple of 32), and as many ring
 // slots as the shared memory of `blocks_per_sm` blocks per SM allows.
@@ -98,6 +94,11 @@ bool tma_shape(int units_row, int vpt, int inputs, int blocks_per_sm, int max_st
     return true;
 }
 
+// One-shot fused shape.  Modes kRegisters / kStaged / kPersistent: threads per
+// row = units_row / vpt rounded up to a power of two; blocks hold at least
+// 128 threads; register-resident rows are limited by the registers a thread
+// may use, staged rows by shared memory.  Mode kTma: tma_shape.  Returns
+// false when the row does not fit (then only the two-shot path can take it).
 bool oneshot_shape(int units_row, int vpt, int lanes, bool packed, int mode, int R, OneShotShape* sh,
                    int blocks_per_sm = 1, int max_stages = 0)
 {
@@ -308,7 +309,6 @@ bool norm_shape(int units_row, bool packed, OneShotShape* sh, int vpt = 0)
     sh->smem_bytes = 0;
     return true;
 }
-
 
 }  // namespace
 

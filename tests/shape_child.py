@@ -48,6 +48,19 @@ def main():
     # a rank count without a compile-time specialisation
     check(workloads.fused_inputs(3, 21, 4096, "fp16", partial_dist=("N", 0.0, 0.3), residual_dist=("N", 0.0, 4.0),
                                  bias_dist=("N", 0.0, 0.02), weight_dist=("N", 1.0, 0.05), eps=1e-5, seed=7))
+    # Aliasing under this shape (persistent kernels prefetch later rows):
+    # out on one of the partials, residual_out on the residual.
+    al = workloads.tp_prefill(tokens=700, seed=8)
+    ref = oracle.residual_rmsnorm(al.partials, al.bias, al.residual, al.weight, al.eps, al.dtype)
+    ap = [p.cuda() for p in al.partials]
+    ares = al.residual.cuda()
+    o, r = ar.ar_residual_rmsnorm(ap, ares, al.weight.cuda(), al.eps, bias=al.bias.cuda(), out=ap[5],
+                                  residual_out=ares, strategy="ONESHOT")
+    torch.cuda.synchronize()
+    assert o.data_ptr() == ap[5].data_ptr() and r.data_ptr() == ares.data_ptr()
+    terms = [p.reshape(700, 8192) for p in al.partials] + [al.bias.expand(700, 8192).contiguous(), al.residual]
+    tol.check_sum(r.cpu(), ref[1], terms, "bf16", "aliased residual_out")
+    tol.check_fused_out(o.cpu(), ref[0], terms, al.weight, ref[2], "bf16", 8192, "aliased out")
     # The norm on its own under the same shape: the register-resident kernel
     # with these units per thread, or the bulk-copy-fed kernel streaming x alone.
     for T, H, dt in [(37, 8192, "bf16"), (21, 8000, "bf16"), (9, 4096, "fp16"), (5, 1024, "fp32")]:

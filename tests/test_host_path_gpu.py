@@ -71,3 +71,18 @@ def test_host_path_repeated_calls_share_nothing_stale():
     b = workloads.tp_prefill(tokens=24, hidden=4096, seed=6)
     for inp in (a, b, a):
         _check(inp, *_run_host(inp, 5))
+
+
+def test_host_path_full_prefill_sampled_rows():
+    """The end-to-end configuration bench.py times: 8192 x 8192 R=8 bf16 with bias on pinned host buffers,
+    512-row chunks, AUTO; sampled rows against the oracle, and residual_out bit for bit with the device call."""
+    inp = workloads.tp_prefill(seed=3)
+    T, H = inp.tokens, inp.hidden
+    out, rout = _run_host(inp, 512)
+    g = torch.Generator().manual_seed(11)
+    rows = sorted(set([0, 511, 512, 4095, 4096, T - 1] + torch.randint(0, T, (16,), generator=g).tolist()))
+    ridx = torch.tensor(rows)
+    sub = workloads.FusedInputs(inp.R, len(rows), H, inp.dtype, inp.eps,
+                                [p[ridx].contiguous() for p in inp.partials], inp.residual[ridx].contiguous(),
+                                inp.weight, inp.bias)
+    _check(sub, out[ridx].contiguous(), rout[ridx].contiguous())
