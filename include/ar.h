@@ -312,7 +312,8 @@ typedef enum {
     AR_KERNEL_ONESHOT_SHARED = 2,     /* k_fused_oneshot, row sums in shared memory */
     AR_KERNEL_ONESHOT_PERSISTENT = 3, /* k_fused_oneshot_persist */
     AR_KERNEL_ONESHOT_BULK = 4,       /* k_fused_oneshot_tma: persistent, fed by bulk copies */
-    AR_KERNEL_TWOSHOT = 5             /* k_twoshot_phase1 then k_twoshot_phase2 */
+    AR_KERNEL_TWOSHOT = 5,            /* k_twoshot_phase1 then k_twoshot_phase2 */
+    AR_KERNEL_ONESHOT_CLUSTER = 6     /* k_fused_oneshot_cluster: a row split across a block cluster */
 } ar_kernel;
 
 /* Launch plan of a fused call (see ar_query_launch). */
@@ -328,6 +329,7 @@ typedef struct {
     int stages;            /* bulk-copy kernel: ring slots per block; else 0 */
     int smem_bytes;        /* dynamic shared memory per block */
     int early_residual;    /* one-shot: residual_out written before the row's norm is known */
+    int cluster;           /* row-split kernel: blocks (one cluster) per row; else 0 */
 } ar_launch_plan;
 
 /*

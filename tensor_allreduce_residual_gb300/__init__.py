@@ -69,12 +69,12 @@ class ArLaunchPlan(ctypes.Structure):
     """Mirror of the C struct ar_launch_plan."""
     _fields_ = [(name, ctypes.c_int) for name in (
         "strategy", "kernel", "threads_per_row", "units_per_thread", "rows_per_block", "threads_per_block",
-        "blocks_per_sm", "stages", "smem_bytes", "early_residual")]
+        "blocks_per_sm", "stages", "smem_bytes", "early_residual", "cluster")]
 
 
 # ar_kernel codes and the kernel names they stand for
 KERNEL_NAMES = {1: "k_fused_oneshot", 2: "k_fused_oneshot", 3: "k_fused_oneshot_persist",
-                4: "k_fused_oneshot_tma", 5: "k_twoshot_phase1+k_twoshot_phase2"}
+                4: "k_fused_oneshot_tma", 5: "k_twoshot_phase1+k_twoshot_phase2", 6: "k_fused_oneshot_cluster"}
 
 _lib: Optional[ctypes.CDLL] = None
 

@@ -94,6 +94,28 @@ bool tma_shape(int units_row, int vpt, int inputs, int blocks_per_sm, int max_st
     return true;
 }
 
+// Row-split shape (mode kCluster): `cluster` blocks share a row, each owning
+// ceil(units_row / cluster) units at `vpt` per thread; threads per block =
+// that over vpt, rounded up to a power of two, at least a warp.
+bool cluster_shape(int units_row, int vpt, int lanes, int cluster, OneShotShape* sh)
+{
+    if (!(vpt == 1 || vpt == 2 || vpt == 4 || vpt == 8) || !(cluster == 2 || cluster == 4 || cluster == 8))
+        return false;
+    const int slice = (units_row + cluster - 1) / cluster;
+    int tpb = next_pow2((slice + vpt - 1) / vpt);
+    if (tpb < 32)
+        tpb = 32;
+    if (tpb > ar::oneshot_max_threads(vpt * lanes))
+        return false;
+    sh->tpr = tpb;
+    sh->vpt = vpt;
+    sh->rows = 1;
+    sh->mode = ar::kCluster;
+    sh->smem_bytes = 0;
+    sh->cluster = cluster;
+    return true;
+}
+
 // One-shot fused shape.  Modes kRegisters / kStaged / kPersistent: threads per
 // row = units_row / vpt rounded up to a power of two; blocks hold at least
 // 128 threads; register-resident rows are limited by the registers a thread
@@ -104,6 +126,8 @@ bool oneshot_shape(int units_row, int vpt, int lanes, bool packed, int mode, int
 {
     if (mode == ar::kTma)
         return packed && tma_shape(units_row, vpt, R + 1, blocks_per_sm, max_stages, sh);
+    if (mode == ar::kCluster)  // blocks_per_sm carries the cluster size for this mode
+        return packed && cluster_shape(units_row, vpt, lanes, blocks_per_sm, sh);
     const int max_vpt = packed ? ar::kMaxVPTVec : ar::kMaxVPTScalar;
     const bool stage = mode != ar::kRegisters;
     if (vpt < 1 || vpt > max_vpt || (stage && (!packed || vpt > ar::kMaxVPTVec)))
@@ -153,6 +177,7 @@ int rule_vpt(int units_row, int tokens, int lanes, bool packed)
 // the row does not fit that kernel.
 constexpr int kTmaRuleMinTokens = 2048;
 constexpr int kTwoShotRuleMinTokens = 1024;
+constexpr int kClusterRuleMaxTokens = 8;
 constexpr size_t kTmaRuleInflight = 144 * 1024;
 
 bool tma_rule_shape(int units_row, int R, OneShotShape* sh)
@@ -182,8 +207,9 @@ const ar::AutoEntry* table_lookup(int esize, int R, int units_row, int tokens)
 // Measurement override of the one-shot shape: AR_ONESHOT_SHAPE="vpt:mode",
 // "vpt:mode:early", "vpt:mode:early:blocks_per_sm" or
 // "vpt:mode:early:blocks_per_sm:max_stages" (e.g. "4:1", "2:0:1", "4:3:0:2",
-// "4:3:1:1:3") replaces the table and the rule for every packed call.  Read
-// once per process; used to sweep shapes when building the AUTO table.
+// "4:3:1:1:3"; for mode 4 the fourth field is the cluster size, "1:4:1:8")
+// replaces the table and the rule for every packed call.  Read once per
+// process; used to sweep shapes when building the AUTO table.
 struct ShapeOverride {
     int vpt = 0;
     int mode = 0;
@@ -199,7 +225,7 @@ const ShapeOverride& shape_override()
         if (const char* env = std::getenv("AR_ONESHOT_SHAPE")) {
             int v = 0, st = 0, early = 0, bps = 1, stages = 0;
             const int got = std::sscanf(env, "%d:%d:%d:%d:%d", &v, &st, &early, &bps, &stages);
-            if (got >= 2 && v > 0 && st >= 0 && st <= ar::kTma) {
+            if (got >= 2 && v > 0 && st >= 0 && st <= ar::kCluster) {
                 o.vpt = v;
                 o.mode = st;
                 o.early = got >= 3 && early != 0;
@@ -253,6 +279,16 @@ FusedPlan plan_fused(int esize, int R, int hidden, int tokens, bool packed, int 
     const bool measured = packed && (table_lookup(esize, R, units_row, tokens) != nullptr || shape_override().vpt > 0);
     if (!measured && packed && tokens >= kTmaRuleMinTokens && tma_rule_shape(units_row, R, &p.shape)) {
         p.shape.early_residual = 1;
+        p.oneshot_ok = true;
+        p.strategy = strategy == AR_AUTO ? AR_ONESHOT : strategy;
+        return p;
+    }
+    // A few long rows: split each across a cluster of 8 blocks (measured at
+    // one token: 3.1 us against 4.0 us for R=8 bf16 H=8192, 3.2 against 4.5
+    // for R=2 bf16 H=16384).
+    if (!measured && packed && tokens <= kClusterRuleMaxTokens && units_row >= 1024 &&
+        cluster_shape(units_row, units_row >= 2048 ? 2 : 1, lanes, 8, &p.shape)) {
+        p.shape.early_residual = 0;
         p.oneshot_ok = true;
         p.strategy = strategy == AR_AUTO ? AR_ONESHOT : strategy;
         return p;
@@ -576,6 +612,14 @@ int ar_query_launch(int R, int hidden, int tokens, int dtype, int strategy, ar_l
             p.kernel = AR_KERNEL_ONESHOT_PERSISTENT;
             p.threads_per_block = sh.tpr;
             break;
+        case ar::kCluster:
+            p.kernel = AR_KERNEL_ONESHOT_CLUSTER;
+            p.threads_per_row = sh.tpr * sh.cluster;
+            p.threads_per_block = sh.tpr;
+            p.blocks_per_sm = 0;
+            p.stages = 0;
+            p.cluster = sh.cluster;
+            break;
         default:
             p.kernel = AR_KERNEL_ONESHOT_BULK;
             p.threads_per_block = sh.tpr + 32;
@@ -691,8 +735,9 @@ int ar_query_strategy(int R, size_t n, int hidden, int dtype, int fusion_op, int
     const bool packed = hidden % (16 / esize) == 0;
     FusedPlan plan = plan_fused(esize, R, hidden, tokens, packed, AR_AUTO);
     *chosen = plan.strategy;
+    const int row_threads = plan.shape.tpr * (plan.shape.mode == ar::kCluster ? plan.shape.cluster : 1);
     if (warps_per_token)
-        *warps_per_token = plan.strategy == AR_ONESHOT ? (plan.shape.tpr + 31) / 32 : 0;
+        *warps_per_token = plan.strategy == AR_ONESHOT ? (row_threads + 31) / 32 : 0;
     return AR_OK;
 }
 

@@ -27,34 +27,34 @@ struct AutoEntry {
 
 static const AutoEntry kAutoTable[] = {
     {2, 2, 512, 1, 1, 1, 0, 1, 1, 0},  // tp_decode_R2_fp16_H4096 T=1: one-shot 2.493 us
-    {2, 2, 512, 2, 1, 1, 0, 1, 1, 0},  // tp_decode_R2_fp16_H4096 T=2: one-shot 2.522 us
-    {2, 2, 512, 4, 1, 2, 0, 1, 1, 0},  // tp_decode_R2_fp16_H4096 T=4: one-shot 2.784 us
-    {2, 2, 512, 8, 1, 1, 0, 0, 1, 0},  // tp_decode_R2_fp16_H4096 T=8: one-shot 2.755 us
-    {2, 2, 512, 16, 1, 1, 0, 1, 1, 0},  // tp_decode_R2_fp16_H4096 T=16: one-shot 2.918 us
-    {2, 2, 512, 32, 1, 1, 0, 1, 1, 0},  // tp_decode_R2_fp16_H4096 T=32: one-shot 2.739 us
-    {2, 2, 512, 64, 1, 1, 0, 1, 1, 0},  // tp_decode_R2_fp16_H4096 T=64: one-shot 2.762 us
-    {2, 2, 512, 256, 1, 2, 0, 1, 1, 0},  // tp_decode_R2_fp16_H4096 T=256: one-shot 3.318 us
+    {2, 2, 512, 2, 1, 1, 0, 1, 1, 0},  // tp_decode_R2_fp16_H4096 T=2: one-shot 2.419 us
+    {2, 2, 512, 4, 1, 1, 0, 1, 1, 0},  // tp_decode_R2_fp16_H4096 T=4: one-shot 2.429 us
+    {2, 2, 512, 8, 1, 1, 0, 1, 1, 0},  // tp_decode_R2_fp16_H4096 T=8: one-shot 2.445 us
+    {2, 2, 512, 16, 1, 1, 0, 1, 1, 0},  // tp_decode_R2_fp16_H4096 T=16: one-shot 2.445 us
+    {2, 2, 512, 32, 1, 2, 0, 1, 1, 0},  // tp_decode_R2_fp16_H4096 T=32: one-shot 2.557 us
+    {2, 2, 512, 64, 1, 1, 0, 1, 1, 0},  // tp_decode_R2_fp16_H4096 T=64: one-shot 2.554 us
+    {2, 2, 512, 256, 1, 2, 0, 1, 1, 0},  // tp_decode_R2_fp16_H4096 T=256: one-shot 3.094 us
     {2, 2, 512, 1024, 1, 2, 0, 1, 1, 0},  // tp_decode_R2_fp16_H4096 T=1024: one-shot 6.112 us
     {2, 2, 512, 2147483647, 1, 1, 0, 1, 1, 0},  // tp_decode_R2_fp16_H4096 T=8192: one-shot 52.349 us
-    {2, 2, 2048, 1, 1, 8, 3, 1, 1, 8},  // R2_bf16_H16384 T=1: one-shot 4.675 us
-    {2, 2, 2048, 64, 1, 2, 0, 1, 1, 0},  // R2_bf16_H16384 T=64: one-shot 5.267 us
+    {2, 2, 2048, 1, 1, 2, 4, 0, 8, 0},  // R2_bf16_H16384 T=1: one-shot 3.187 us
+    {2, 2, 2048, 64, 1, 2, 4, 1, 4, 0},  // R2_bf16_H16384 T=64: one-shot 4.422 us
     {2, 2, 2048, 1024, 2, 0, 0, 0, 1, 0},  // R2_bf16_H16384 T=1024: two-shot 29.686 us
     {2, 2, 2048, 2147483647, 2, 0, 0, 0, 1, 0},  // R2_bf16_H16384 T=4096: two-shot 120.256 us
-    {2, 4, 1024, 1, 1, 2, 0, 1, 1, 0},  // R4_fp16_H8192 T=1: one-shot 3.606 us
-    {2, 4, 1024, 64, 1, 2, 0, 1, 1, 0},  // R4_fp16_H8192 T=64: one-shot 3.626 us
+    {2, 4, 1024, 1, 1, 1, 4, 0, 8, 0},  // R4_fp16_H8192 T=1: one-shot 3.123 us
+    {2, 4, 1024, 64, 1, 2, 0, 1, 1, 0},  // R4_fp16_H8192 T=64: one-shot 3.414 us
     {2, 4, 1024, 1024, 1, 1, 3, 1, 1, 8},  // R4_fp16_H8192 T=1024: one-shot 18.016 us
     {2, 4, 1024, 4096, 1, 4, 3, 1, 1, 4},  // R4_fp16_H8192 T=4096: one-shot 70.666 us
     {2, 4, 1024, 2147483647, 1, 4, 3, 1, 1, 4},  // R4_fp16_H8192 T=8192: one-shot 137.034 us
-    {2, 8, 512, 1, 1, 1, 0, 1, 1, 0},  // R8_bf16_H4096 T=1: one-shot 3.363 us
-    {2, 8, 512, 64, 1, 1, 0, 1, 1, 0},  // R8_bf16_H4096 T=64: one-shot 3.466 us
+    {2, 8, 512, 1, 1, 1, 4, 0, 8, 0},  // R8_bf16_H4096 T=1: one-shot 2.966 us
+    {2, 8, 512, 64, 1, 1, 0, 1, 1, 0},  // R8_bf16_H4096 T=64: one-shot 3.085 us
     {2, 8, 512, 1024, 1, 1, 3, 1, 1, 8},  // R8_bf16_H4096 T=1024: one-shot 12.307 us
     {2, 8, 512, 4096, 1, 1, 3, 1, 1, 2},  // R8_bf16_H4096 T=4096: one-shot 55.19 us
     {2, 8, 512, 2147483647, 1, 1, 3, 1, 1, 2},  // R8_bf16_H4096 T=8192: one-shot 106.445 us
-    {2, 8, 1024, 1, 1, 2, 0, 1, 1, 0},  // R8_bf16_H8192 T=1: one-shot 3.971 us
-    {2, 8, 1024, 8, 1, 2, 0, 1, 1, 0},  // R8_bf16_H8192 T=8: one-shot 4.218 us
-    {2, 8, 1024, 32, 1, 2, 0, 1, 1, 0},  // R8_bf16_H8192 T=32: one-shot 4.16 us
-    {2, 8, 1024, 64, 1, 2, 0, 1, 1, 0},  // R8_bf16_H8192 T=64: one-shot 4.211 us
-    {2, 8, 1024, 256, 1, 2, 0, 1, 1, 0},  // R8_bf16_H8192 T=256: one-shot 6.016 us
+    {2, 8, 1024, 1, 1, 1, 4, 0, 8, 0},  // R8_bf16_H8192 T=1: one-shot 3.107 us
+    {2, 8, 1024, 8, 1, 1, 4, 1, 8, 0},  // R8_bf16_H8192 T=8: one-shot 3.325 us
+    {2, 8, 1024, 32, 1, 1, 4, 1, 8, 0},  // R8_bf16_H8192 T=32: one-shot 3.779 us
+    {2, 8, 1024, 64, 1, 2, 0, 1, 1, 0},  // R8_bf16_H8192 T=64: one-shot 3.968 us
+    {2, 8, 1024, 256, 1, 2, 0, 1, 1, 0},  // R8_bf16_H8192 T=256: one-shot 5.68 us
     {2, 8, 1024, 512, 1, 2, 3, 1, 1, 0},  // R8_bf16_H8192 T=512: one-shot 12.717 us
     {2, 8, 1024, 1024, 1, 4, 1, 0, 1, 0},  // R8_bf16_H8192 T=1024: one-shot 29.632 us
     {2, 8, 1024, 2048, 1, 4, 3, 1, 1, 4},  // R8_bf16_H8192 T=2048: one-shot 55.331 us

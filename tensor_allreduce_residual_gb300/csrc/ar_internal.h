@@ -79,8 +79,12 @@ enum OneShotMode {
     kRegisters = 0,   // registers, one block per `rows` rows
     kStaged = 1,      // shared memory, one block per `rows` rows
     kPersistent = 2,  // shared memory, persistent blocks striding over rows
-    kTma = 3          // registers, persistent blocks fed by bulk copies into a shared-memory ring
+    kTma = 3,         // registers, persistent blocks fed by bulk copies into a shared-memory ring
+    kCluster = 4      // registers, each row split across a thread-block cluster
 };
+
+// Cluster sizes the row-split one-shot kernel may use (portable limit 8).
+constexpr int kMaxCluster = 8;
 
 // One-shot fused launch shape: `tpr` threads per row (a power of two),
 // `vpt` units per thread, `rows` rows per block, the mode, the dynamic
@@ -94,6 +98,7 @@ struct OneShotShape {
     int early_residual;  // write residual_out before the row barrier
     int stages;          // kTma: ring slots per block
     int blocks_per_sm;   // kTma: resident blocks per SM
+    int cluster;         // kCluster: blocks per row (the cluster size); tpr is then threads per block
 };
 
 // Largest block of the persistent one-shot kernel (it keeps the next row's

@@ -13,6 +13,7 @@
 // pointers, a single element.
 #pragma once
 
+#include <cooperative_groups.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <stdint.h>
@@ -441,6 +442,90 @@ k_fused_oneshot(const FusedArgs a, const int tpr)
             U::store(a.out, row_off + j, y);
         }
     }
+}
+
+// ---------------------------------------------------------------------------
+// A4 for few rows: one row split across a thread-block cluster of C blocks.
+// With one block per row, a single SM streams the whole row (R + 1 inputs of
+// hidden elements), which bounds decode latency.  Here block c of the
+// cluster of row t owns the contiguous slice [c*S, (c+1)*S) of the row's
+// units (S = ceil(units_row / C)), keeps its x in registers, and reduces its
+// slice's sum of squares; the C partial sums are exchanged through
+// distributed shared memory between two cluster barriers and added in
+// cluster-rank order (fixed, so deterministic).  The second barrier keeps
+// every block's shared memory alive until all have read it.  Cluster
+// barriers are hardware barriers over co-scheduled blocks: no spin loop.
+// Packed path; grid = tokens * C blocks of `blockDim.x` threads, cluster (C).
+// ---------------------------------------------------------------------------
+template <typename T, int R_CT, int VPT>
+__global__ void __launch_bounds__(oneshot_max_threads(VPT * Lanes<T>::V))
+k_fused_oneshot_cluster(const FusedArgs a, const int csize)
+{
+    pdl_enter();
+    namespace cg = cooperative_groups;
+    using U = Unit<T, true>;
+    constexpr int L = U::L;
+    __shared__ float red[32];
+    __shared__ float part;  // this block's partial sum of squares
+
+    cg::cluster_group cluster = cg::this_cluster();
+    const int crank = static_cast<int>(cluster.block_rank());
+    const int row = static_cast<int>(blockIdx.x) / csize;
+    const int slice = (a.units_row + csize - 1) / csize;
+    const int j_begin = crank * slice;
+    const int j_end = min(j_begin + slice, a.units_row);
+    const uint64_t row_off = static_cast<uint64_t>(row) * a.units_row;
+    const int tpb = static_cast<int>(blockDim.x);
+
+    float x[VPT][L];
+    typename U::raw wv[VPT];
+    float ss = 0.0f;
+#pragma unroll
+    for (int k = 0; k < VPT; ++k) {
+        const int j = j_begin + static_cast<int>(threadIdx.x) + k * tpb;
+#pragma unroll
+        for (int l = 0; l < L; ++l)
+            x[k][l] = 0.0f;
+        if (j < j_end) {
+            sum_partials<T, true, R_CT>(a.partials, a.R, row_off + j, x[k]);
+            float t[L];
+            if (a.bias != nullptr) {
+                U::to_float(U::load_cached(a.bias, j), t);
+                add_lanes<L>(x[k], t);
+            }
+            U::to_float(U::load(a.residual, row_off + j), t);
+            add_lanes<L>(x[k], t);
+            wv[k] = U::load_cached(a.weight, j);
+            if (a.early_residual)
+                U::store(a.residual_out, row_off + j, x[k]);
+#pragma unroll
+            for (int l = 0; l < L; ++l)
+                ss = fmaf(x[k][l], x[k][l], ss);
+        }
+    }
+    ss = row_sum(ss, tpb, red);
+    if (threadIdx.x == 0)
+        part = ss;
+    cluster.sync();
+    float tot = 0.0f;
+    for (int c = 0; c < csize; ++c)
+        tot += *cluster.map_shared_rank(&part, c);
+    const float inv = inv_rms(tot, a.hidden, a.eps);
+#pragma unroll
+    for (int k = 0; k < VPT; ++k) {
+        const int j = j_begin + static_cast<int>(threadIdx.x) + k * tpb;
+        if (j < j_end) {
+            if (!a.early_residual)
+                U::store(a.residual_out, row_off + j, x[k]);
+            float w[L], y[L];
+            U::to_float(wv[k], w);
+#pragma unroll
+            for (int l = 0; l < L; ++l)
+                y[l] = x[k][l] * inv * w[l];
+            U::store(a.out, row_off + j, y);
+        }
+    }
+    cluster.sync();  // no block leaves while another may still read its `part`
 }
 
 // ---------------------------------------------------------------------------

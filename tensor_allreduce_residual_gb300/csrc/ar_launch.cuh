@@ -79,6 +79,39 @@ cudaError_t launch_sum(const SumArgs& a, bool packed, int nslices, cudaStream_t 
     }
 }
 
+// Same as launch_k, with the blocks grouped into clusters of `cluster_x`.
+template <typename... KArgs, typename... Args>
+static cudaError_t launch_k_cluster(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                                    unsigned cluster_x, Args&&... args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = cluster_x;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl_enabled() ? 2 : 1;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
+// One row per cluster of sh.cluster blocks of sh.tpr threads.
+template <typename T, int R_CT, int VPT>
+static cudaError_t run_cluster(const FusedArgs& a, OneShotShape sh, cudaStream_t s)
+{
+    const long long blocks = static_cast<long long>(a.tokens) * sh.cluster;
+    if (blocks > INT_MAX || sh.cluster < 1 || sh.cluster > kMaxCluster)
+        return cudaErrorInvalidConfiguration;
+    return launch_k_cluster(k_fused_oneshot_cluster<T, R_CT, VPT>, dim3(static_cast<unsigned>(blocks)),
+                            dim3(sh.tpr), 0, s, static_cast<unsigned>(sh.cluster), a, sh.cluster);
+}
+
 template <typename T, bool PACKED, int R_CT, int VPT, bool STAGE, bool EARLY>
 static cudaError_t run_oneshot(const FusedArgs& a, OneShotShape sh, cudaStream_t s)
 {
@@ -165,6 +198,15 @@ static cudaError_t run_tma(const FusedArgs& a, OneShotShape sh, cudaStream_t s)
 template <typename T, int R_CT>
 static cudaError_t oneshot_packed(const FusedArgs& a, OneShotShape sh, cudaStream_t s)
 {
+    if (sh.mode == kCluster) {
+        switch (sh.vpt) {
+        case 1: return run_cluster<T, R_CT, 1>(a, sh, s);
+        case 2: return run_cluster<T, R_CT, 2>(a, sh, s);
+        case 4: return run_cluster<T, R_CT, 4>(a, sh, s);
+        case 8: return run_cluster<T, R_CT, 8>(a, sh, s);
+        default: return cudaErrorInvalidValue;
+        }
+    }
     if (sh.mode == kTma) {
         switch (sh.vpt) {
         case 1: return run_tma<T, R_CT, 1>(a, sh, s);

@@ -34,7 +34,8 @@ CASES = [
 ]
 SHAPES = ([f"{v}:{m}:{e}" for v in (1, 2, 4, 8) for m in (0, 1) for e in (0, 1)]
           + [f"{v}:2:{e}" for v in (2, 4) for e in (0, 1)]
-          + [f"{v}:3:{e}:{b}" for v in (1, 2, 4, 8) for e in (0, 1) for b in (1, 2)])
+          + [f"{v}:3:{e}:{b}" for v in (1, 2, 4, 8) for e in (0, 1) for b in (1, 2)]
+          + [f"{v}:4:1:{c}" for v in (1, 2, 4) for c in (2, 4, 8)])
 
 
 def _graph_time(torch, fn, n=10, reps=5):

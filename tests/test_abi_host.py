@@ -151,10 +151,11 @@ def test_twoshot_workspace_errors(L):
     assert _fused(L, strategy=ar.AR_TWOSHOT, ws=None) == ar.AR_ERR_WORKSPACE
     assert _fused(L, strategy=ar.AR_TWOSHOT, ws=FAKE + 6 << 20, ws_bytes=0) == ar.AR_ERR_WORKSPACE
     assert _fused(L, strategy=ar.AR_TWOSHOT, ws=FAKE + (6 << 20) + 2, ws_bytes=need) == ar.AR_ERR_WORKSPACE
-    # a row too long for the one-shot kernel: ONESHOT is unsupported, AUTO needs a workspace
+    # a row too long for every one-shot kernel at 64 tokens (the row-split cluster kernel
+    # takes long rows only for a few tokens): ONESHOT is unsupported, AUTO needs a workspace
     long_row = 8 * 4096 * 2  # fp32 lanes * units per thread * threads, beyond the register budget
-    assert _fused(L, hidden=long_row, strategy=ar.AR_ONESHOT) == ar.AR_ERR_UNSUPPORTED
-    assert _fused(L, hidden=long_row, strategy=ar.AR_AUTO) == ar.AR_ERR_WORKSPACE
+    assert _fused(L, hidden=long_row, tokens=64, strategy=ar.AR_ONESHOT) == ar.AR_ERR_UNSUPPORTED
+    assert _fused(L, hidden=long_row, tokens=64, strategy=ar.AR_AUTO) == ar.AR_ERR_WORKSPACE
 
 
 def test_fused_empty_is_noop(L):

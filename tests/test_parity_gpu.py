@@ -263,14 +263,22 @@ def test_fused_generic_rank_counts(R, dtype):
 
 
 def test_row_too_long_for_one_shot():
-    f = workloads.fused_inputs(2, 3, 40960, "bf16", partial_dist=("N", 0.0, 0.5), residual_dist=("N", 0.0, 4.0),
-                               bias_dist=("N", 0.0, 0.02), weight_dist=("N", 1.0, 0.05), eps=1e-6, seed=9)
+    """A 40960-wide bf16 row (5120 vectors): at 3 tokens the row-split cluster kernel holds it (one
+    row over 8 blocks); at 16 tokens no one-shot kernel does, and only the two-shot path runs."""
+    few = workloads.fused_inputs(2, 3, 40960, "bf16", partial_dist=("N", 0.0, 0.5), residual_dist=("N", 0.0, 4.0),
+                                 bias_dist=("N", 0.0, 0.02), weight_dist=("N", 1.0, 0.05), eps=1e-6, seed=9)
+    assert ar.ar_query_launch(2, 40960, 3, ar.AR_BF16, "ONESHOT")["kernel_name"] == "k_fused_oneshot_cluster"
+    for s in STRATS:
+        out, res = run_fused(few, s)
+        check_fused(few, out, res)
+    many = workloads.fused_inputs(2, 16, 40960, "bf16", partial_dist=("N", 0.0, 0.5), residual_dist=("N", 0.0, 4.0),
+                                  bias_dist=("N", 0.0, 0.02), weight_dist=("N", 1.0, 0.05), eps=1e-6, seed=10)
     with pytest.raises(ar.ARError) as e:
-        run_fused(f, "ONESHOT")
+        run_fused(many, "ONESHOT")
     assert e.value.status == ar.AR_ERR_UNSUPPORTED
     for s in ["TWOSHOT", "AUTO"]:
-        out, res = run_fused(f, s)
-        check_fused(f, out, res)
+        out, res = run_fused(many, s)
+        check_fused(many, out, res)
 
 
 @pytest.mark.parametrize("strategy", STRATS)
