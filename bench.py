@@ -258,12 +258,13 @@ def run_ours(args, rank, world, local_rank):
     # End to end through the C ABI on HOST buffers: every step,
     # ar_residual_rmsnorm_host copies that step's inputs from pinned host
     # memory, runs the fused kernels and copies both outputs back, in chunks
-    # of 512 rows with the copies overlapping the kernels.  Timed on the
-    # stream until the outputs are in host memory.
+    # of 1024 rows with the copies overlapping the kernels (1024-row chunks
+    # measured 227.5 GB/s against 224.1 for 512 and 213.4 for 256).  Timed on
+    # the stream until the outputs are in host memory.
     host_parts = [t.cpu().pin_memory() for t in parts]
     host_res, host_w, host_b = (t.cpu().pin_memory() for t in (resid, weight, bias))
     host_out = [torch.empty(out.shape, dtype=out.dtype).pin_memory() for _ in range(2)]
-    chunk = 512
+    chunk = 1024
     staging = torch.empty(ar.ar_host_staging_size(R, HIDDEN, chunk, ar.AR_BF16), dtype=torch.uint8, device=dev)
     h2d = sum(t.numel() * t.element_size() for t in host_parts + [host_res, host_w, host_b])
     d2h = sum(t.numel() * t.element_size() for t in host_out)
