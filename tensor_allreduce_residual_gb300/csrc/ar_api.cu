@@ -155,12 +155,13 @@ bool oneshot_shape(int units_row, int vpt, int lanes, bool packed, int mode, int
 }
 
 // Rule used when the measured table has no entry: aim for 512 threads per
-// row when there are few rows (more memory parallelism per row) and 256
-// otherwise, with the smallest units-per-thread that reaches it.
+// row up to 512 rows (every measured row shape was fastest near 512 threads
+// per row there: fewer registers per thread, more loads in flight per row)
+// and 256 beyond, with the smallest units-per-thread that reaches it.
 int rule_vpt(int units_row, int tokens, int lanes, bool packed)
 {
     const int max_vpt = packed ? ar::kMaxVPTVec : ar::kMaxVPTScalar;
-    const int target = tokens <= 32 ? 512 : 256;
+    const int target = tokens <= 512 ? 512 : 256;
     int vpt = 1;
     while (vpt < max_vpt && (units_row + vpt - 1) / vpt > target)
         vpt <<= 1;
@@ -185,12 +186,18 @@ bool tma_rule_shape(int units_row, int R, OneShotShape* sh)
     int cpr = 1;
     while (cpr < 8 && (units_row + cpr - 1) / cpr > ar::tma_max_consumers(cpr))
         cpr <<= 1;
-    const int nc = ((units_row + cpr - 1) / cpr + 31) / 32 * 32;
-    const size_t stage = static_cast<size_t>(R + 1) * nc * 16;
-    int stages = static_cast<int>((kTmaRuleInflight + stage / 2) / stage);
-    if (stages < ar::kTmaMinStages)
-        stages = ar::kTmaMinStages;
-    return tma_shape(units_row, cpr, R + 1, 1, stages, sh);
+    // With many partials a stage of (R + 1) chunks can outgrow the ring: cut
+    // the row into more, smaller chunks until two stages fit the budget.
+    for (; cpr <= 8; cpr <<= 1) {
+        const int nc = ((units_row + cpr - 1) / cpr + 31) / 32 * 32;
+        const size_t stage = static_cast<size_t>(R + 1) * nc * 16;
+        int stages = static_cast<int>((kTmaRuleInflight + stage / 2) / stage);
+        if (stages < ar::kTmaMinStages)
+            stages = ar::kTmaMinStages;
+        if (tma_shape(units_row, cpr, R + 1, 1, stages, sh))
+            return true;
+    }
+    return false;
 }
 
 const ar::AutoEntry* table_lookup(int esize, int R, int units_row, int tokens)

@@ -40,6 +40,10 @@ static const AutoEntry kAutoTable[] = {
     {2, 2, 2048, 64, 1, 2, 4, 1, 4, 0},  // R2_bf16_H16384 T=64: one-shot 4.422 us
     {2, 2, 2048, 1024, 2, 0, 0, 0, 1, 0},  // R2_bf16_H16384 T=1024: two-shot 29.686 us
     {2, 2, 2048, 2147483647, 2, 0, 0, 0, 1, 0},  // R2_bf16_H16384 T=4096: two-shot 120.256 us
+    {2, 3, 512, 1, 1, 1, 0, 1, 1, 0},  // R3_fp16_H4096 T=1: one-shot 2.902 us
+    {2, 3, 512, 64, 1, 1, 3, 1, 1, 2},  // R3_fp16_H4096 T=64: one-shot 2.979 us
+    {2, 3, 512, 2048, 1, 1, 0, 1, 1, 0},  // R3_fp16_H4096 T=2048: one-shot 17.574 us
+    {2, 3, 512, 2147483647, 1, 1, 3, 1, 1, 4},  // R3_fp16_H4096 T=8192: one-shot 62.422 us
     {2, 4, 1024, 1, 1, 1, 4, 0, 8, 0},  // R4_fp16_H8192 T=1: one-shot 3.123 us
     {2, 4, 1024, 64, 1, 2, 0, 1, 1, 0},  // R4_fp16_H8192 T=64: one-shot 3.414 us
     {2, 4, 1024, 1024, 1, 1, 3, 1, 1, 8},  // R4_fp16_H8192 T=1024: one-shot 18.016 us
@@ -60,6 +64,10 @@ static const AutoEntry kAutoTable[] = {
     {2, 8, 1024, 2048, 1, 4, 3, 1, 1, 4},  // R8_bf16_H8192 T=2048: one-shot 55.331 us
     {2, 8, 1024, 4096, 1, 2, 3, 1, 1, 2},  // R8_bf16_H8192 T=4096: one-shot 106.141 us
     {2, 8, 1024, 2147483647, 1, 2, 3, 1, 1, 2},  // R8_bf16_H8192 T=8192: one-shot 207.29 us
+    {2, 16, 1024, 1, 1, 1, 4, 1, 8, 0},  // R16_bf16_H8192 T=1: one-shot 4.848 us
+    {2, 16, 1024, 64, 1, 1, 4, 1, 4, 0},  // R16_bf16_H8192 T=64: one-shot 5.734 us
+    {2, 16, 1024, 2048, 1, 4, 3, 1, 1, 2},  // R16_bf16_H8192 T=2048: one-shot 95.837 us
+    {2, 16, 1024, 2147483647, 1, 4, 3, 1, 1, 2},  // R16_bf16_H8192 T=8192: one-shot 363.971 us
     {0, 0, 0, 0, 0, 0, 0, 0, 0, 0},  // sentinel
 };
 

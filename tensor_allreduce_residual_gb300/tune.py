@@ -31,6 +31,8 @@ CASES = [
     ("R4_fp16_H8192", 4, "fp16", 8192, True, [1, 64, 1024, 4096, 8192]),
     ("R8_bf16_H4096", 8, "bf16", 4096, True, [1, 64, 1024, 4096, 8192]),
     ("R2_bf16_H16384", 2, "bf16", 16384, True, [1, 64, 1024, 4096]),
+    ("R16_bf16_H8192", 16, "bf16", 8192, True, [1, 64, 2048, 8192]),
+    ("R3_fp16_H4096", 3, "fp16", 4096, True, [1, 64, 2048, 8192]),
 ]
 SHAPES = ([f"{v}:{m}:{e}" for v in (1, 2, 4, 8) for m in (0, 1) for e in (0, 1)]
           + [f"{v}:2:{e}" for v in (2, 4) for e in (0, 1)]
