@@ -452,10 +452,18 @@ def run_extras(ar, torch, workloads, parts, resid, weight, bias, out, res_out, w
                                                                  out=o, residual_out=r, intermediate=w8,
                                                                  strategy="AUTO")
         b = algorithmic_bytes(8, T, 8192, 2, has_bias=False)
+        graph = {}   # the three strategies back to back, before any L2 flush
+        for s in ("ONESHOT", "TWOSHOT", "AUTO"):
+            graph[s] = _time_graph(torch, lambda f=f, o=o, r=r, w8=w8, s=s: ar.ar_residual_rmsnorm(
+                f.partials, f.residual, f.weight, f.eps, out=o, residual_out=r, intermediate=w8, strategy=s)) * 1e3
         cold = _time_cold(torch, fn, stream, flush, 30)
         r8[f"T{T}"] = {"us_warm": round(_time_calls(torch, fn, stream, 100) * 1e3, 2), "us_cold": round(cold * 1e3, 2),
-                       "GBps_cold": round(b / cold / 1e6, 1), "us_graph": round(_time_graph(torch, fn) * 1e3, 2),
+                       "GBps_cold": round(b / cold / 1e6, 1), "us_graph": round(graph["AUTO"], 2),
+                       "us_graph_oneshot": round(graph["ONESHOT"], 2), "us_graph_twoshot": round(graph["TWOSHOT"], 2),
+                       "us_graph_after_flush": round(_time_graph(torch, fn) * 1e3, 2),
                        "auto": ar.STRATEGY_NAMES[ar.ar_query_strategy(8, T * 8192, 8192, ar.AR_BF16)[0]]}
+    for v in r8.values():   # AUTO against the better fixed strategy (graph replay)
+        v["auto_over_best_fixed"] = round(v["us_graph"] / min(v["us_graph_oneshot"], v["us_graph_twoshot"]), 3)
     ex["decode_R8_bf16_H8192"] = r8
     del flush
     # Reduce-only sweep, R=4 fp16, n = 2^9 .. 2^27: device time per call

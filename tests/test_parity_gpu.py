@@ -466,3 +466,17 @@ def test_measured_rank_counts_through_auto(R, dtype, H, T):
     assert kernel in ("k_fused_oneshot_cluster", "k_fused_oneshot_tma", "k_fused_oneshot"), kernel
     out, res = run_fused(f, "AUTO")
     check_fused(f, out, res)
+
+
+@pytest.mark.parametrize("strategy", STRATS)
+def test_permuted_partials_stay_within_tolerance(strategy):
+    """The sum is accumulated in rank order, so permuting the partials changes the fp32 rounding, but
+    never beyond the tolerance around the (permutation-invariant) exact result; residual_out and out
+    of the permuted call are checked against the oracle of the original order."""
+    f = workloads.decode_r8(64, seed=12)
+    ref = oracle.residual_rmsnorm(f.partials, f.bias, f.residual, f.weight, f.eps, f.dtype)
+    for perm in ([7, 6, 5, 4, 3, 2, 1, 0], [3, 0, 6, 1, 7, 4, 2, 5]):
+        g = workloads.FusedInputs(f.R, f.tokens, f.hidden, f.dtype, f.eps, [f.partials[k] for k in perm],
+                                  f.residual, f.weight, f.bias)
+        out, res = run_fused(g, strategy)
+        check_fused(f, out, res, ref)
