@@ -310,3 +310,41 @@ def test_allreduce_config_errors_and_sizes(L):
     assert L.ar_allreduce_config(ctypes.byref(p), 0, ar.AR_ONESHOT, 1, None) == ar.AR_ERR_INVALID_ARG
     p.n = 0
     assert L.ar_allreduce_config(ctypes.byref(p), 0, ar.AR_ONESHOT, 1, None) == ar.AR_OK
+
+
+def test_launch_plans_are_launchable_for_random_shapes(L):
+    """Every plan the host logic accepts, over random shapes, fits the device's launch limits and
+    covers its row; shapes it cannot serve are refused with a status, never a bad plan."""
+    import random
+    rng = random.Random(1234)
+    lanes_of = {ar.AR_FP32: 4, ar.AR_FP16: 8, ar.AR_BF16: 8}
+    seen = set()
+    for _ in range(3000):
+        R = rng.randint(1, 16)
+        dt = rng.choice([ar.AR_FP32, ar.AR_FP16, ar.AR_BF16])
+        hidden = rng.choice([rng.randint(1, 300), rng.randint(1, 70000), 8 * rng.randint(1, 8192)])
+        tokens = rng.choice([rng.randint(1, 40), rng.randint(1, 20000)])
+        strategy = rng.choice([ar.AR_ONESHOT, ar.AR_TWOSHOT, ar.AR_AUTO])
+        plan = ar.ArLaunchPlan()
+        st = L.ar_query_launch(R, hidden, tokens, dt, strategy, ctypes.byref(plan))
+        if st != ar.AR_OK:
+            assert st == ar.AR_ERR_UNSUPPORTED and strategy == ar.AR_ONESHOT, (R, hidden, tokens, dt, strategy, st)
+            continue
+        p = {k: getattr(plan, k) for k, _ in ar.ArLaunchPlan._fields_}
+        seen.add(p["kernel"])
+        assert p["strategy"] in (ar.AR_ONESHOT, ar.AR_TWOSHOT)
+        assert strategy == ar.AR_AUTO or p["strategy"] == strategy
+        assert 32 <= p["threads_per_block"] <= 1024, p
+        assert p["smem_bytes"] <= 227 * 1024, p
+        units = hidden // lanes_of[dt] if hidden % lanes_of[dt] == 0 else hidden
+        if p["kernel"] == 4:       # bulk-copy ring: consumers + producer warp, whole chunks, two stages at least
+            assert p["threads_per_block"] == p["threads_per_row"] + 32 and p["threads_per_row"] % 32 == 0
+            assert p["threads_per_row"] * p["units_per_thread"] >= units and p["stages"] >= 2
+            assert p["smem_bytes"] * p["blocks_per_sm"] <= 228 * 1024 - 1024 * p["blocks_per_sm"]
+        elif p["kernel"] == 6:     # row split over a cluster
+            assert p["cluster"] in (2, 4, 8) and p["threads_per_row"] == p["threads_per_block"] * p["cluster"]
+            assert p["threads_per_row"] * p["units_per_thread"] >= units
+        elif p["kernel"] in (1, 2, 3):
+            assert p["threads_per_row"] * p["units_per_thread"] >= units
+            assert p["threads_per_row"] & (p["threads_per_row"] - 1) == 0
+    assert {1, 4, 5, 6} <= seen, seen      # the draw reached the main kernels
