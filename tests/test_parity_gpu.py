@@ -329,10 +329,16 @@ def test_allreduce_dispatch_matches_direct_calls():
     assert torch.equal(bits(o1), bits(o2)) and torch.equal(bits(r1), bits(r2))
 
 
-@pytest.mark.parametrize("strategy", STRATS)
-def test_guard_bands_untouched_and_inputs_unchanged(strategy):
-    f = workloads.fused_inputs(4, 33, 1000, "bf16", partial_dist=("N", 0.0, 0.25), residual_dist=("N", 0.0, 4.0),
+@pytest.mark.parametrize("strategy,R,T,H,kernel", [
+    ("ONESHOT", 4, 33, 1000, None), ("TWOSHOT", 4, 33, 1000, None), ("AUTO", 4, 33, 1000, None),
+    # the persistent bulk-copy-fed kernel (ragged last chunk: 1000 vectors in chunks of 512) and the
+    # row-split cluster kernel (ragged slices: 1025 vectors over 8 blocks)
+    ("AUTO", 8, 2100, 8000, "k_fused_oneshot_tma"), ("AUTO", 8, 3, 8200, "k_fused_oneshot_cluster")])
+def test_guard_bands_untouched_and_inputs_unchanged(strategy, R, T, H, kernel):
+    f = workloads.fused_inputs(R, T, H, "bf16", partial_dist=("N", 0.0, 0.25), residual_dist=("N", 0.0, 4.0),
                                bias_dist=("N", 0.0, 0.02), weight_dist=("N", 1.0, 0.05), eps=1e-6, seed=13)
+    if kernel is not None:
+        assert ar.ar_query_launch(R, H, T, ar.AR_BF16, strategy)["kernel_name"] == kernel
     n, G = f.tokens * f.hidden, 4096
     bufs = []
     views = []
@@ -341,7 +347,7 @@ def test_guard_bands_untouched_and_inputs_unchanged(strategy):
         b.fill_(-23131)                         # 0xA5A5 pattern
         bufs.append(b)
         views.append(b[G:G + n].view(torch.bfloat16).view(f.tokens, f.hidden))
-    ws_need = ar.ar_workspace_size_rows(4, f.hidden, f.tokens, ar.AR_BF16)
+    ws_need = ar.ar_workspace_size_rows(R, f.hidden, f.tokens, ar.AR_BF16)
     ws = torch.full((ws_need + 2 * G,), 0xA5, dtype=torch.uint8, device="cuda")
     parts = [dev(p) for p in f.partials]
     before = [p.clone() for p in parts] + [dev(f.residual)]
