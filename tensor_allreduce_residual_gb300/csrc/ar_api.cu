@@ -245,6 +245,21 @@ const ShapeOverride& shape_override()
     return ov;
 }
 
+// Test-only fault injection for the bulk-copy-fed kernel's bounded waits:
+// AR_TEST_STALL_STAGE=k makes its producer leave stage k of every block
+// unarmed, so the waits on it run out (about a second) and the kernel takes
+// its abort path; ar_device_status then reports AR_ERR_TIMEOUT.  Read once
+// per process; unset means no stall.
+int test_stall_stage()
+{
+    static const int v = [] {
+        const char* e = std::getenv("AR_TEST_STALL_STAGE");
+        const int k = e != nullptr ? std::atoi(e) : -1;
+        return k >= 0 ? k + 1 : 0;
+    }();
+    return v;
+}
+
 struct FusedPlan {
     int strategy;      // AR_ONESHOT or AR_TWOSHOT
     bool oneshot_ok;   // the row fits the one-shot kernel
@@ -498,6 +513,7 @@ int ar_residual_rmsnorm(const void* const* partials, int R, const void* bias, co
     a.chunk_units = ar::kFlatThreads * ar::kChunkVPT;
     a.eps = eps;
     a.early_residual = plan.shape.early_residual;
+    a.stall_stage = test_stall_stage();
 
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     return status_of(by_dtype(dtype, [&](auto tag) {

@@ -71,6 +71,8 @@ struct FusedArgs {
     int chunk_units;       // two-shot units per chunk
     float eps;
     int early_residual;    // one-shot: write residual_out before the row barrier
+    int stall_stage;       // tests only: the bulk-copy producer leaves stage (stall_stage - 1)
+                           // of every block unarmed; 0 (the zero-initialised value) = none
 };
 
 // Where the one-shot fused kernel keeps a row's fp32 sums between the sum and

@@ -23,9 +23,10 @@
 //
 // Waits are bounded: an mbarrier wait gives up after kWaitLimitNs of
 // %globaltimer time, counts the event in g_wait_timeouts (read by the host
-// through take_wait_timeouts), and the block winds down -- consumers agree
-// at the row barrier to stop, and the producer waits (again bounded) for the
-// copies it issued before it exits.
+// through take_wait_timeouts), and the block winds down -- a consumer warp
+// that gave up releases no further slot, the consumers agree at the row
+// barrier to stop, the producer's own wait for a release runs out, and it
+// waits (again bounded) for the copies it issued before it exits.
 #pragma once
 
 #include "ar_kernels.cuh"
@@ -173,14 +174,18 @@ k_fused_oneshot_tma(const FusedArgs a, const int stages)
                 }
                 const int j0 = c * nc;
                 const uint32_t bytes = static_cast<uint32_t>(min(nc, a.units_row - j0)) * 16u;
-                mbar_arrive_expect_tx(&full[s], bytes * static_cast<uint32_t>(inputs));
-                uint4* dst = ring + static_cast<size_t>(s) * slot_vecs;
-                for (int r = 0; r < R; ++r)
-                    bulk_copy_g2s(dst + static_cast<size_t>(r) * nc,
-                                  static_cast<const uint4*>(a.partials[r]) + row_off + j0, bytes, &full[s]);
-                if (has_res)
-                    bulk_copy_g2s(dst + static_cast<size_t>(R) * nc,
-                                  static_cast<const uint4*>(a.residual) + row_off + j0, bytes, &full[s]);
+                // a.stall_stage (tests only, 0 otherwise) leaves one stage unarmed,
+                // so the waits on it run out and the abort path below is exercised.
+                if (static_cast<uint32_t>(a.stall_stage) != it + 1u) {
+                    mbar_arrive_expect_tx(&full[s], bytes * static_cast<uint32_t>(inputs));
+                    uint4* dst = ring + static_cast<size_t>(s) * slot_vecs;
+                    for (int r = 0; r < R; ++r)
+                        bulk_copy_g2s(dst + static_cast<size_t>(r) * nc,
+                                      static_cast<const uint4*>(a.partials[r]) + row_off + j0, bytes, &full[s]);
+                    if (has_res)
+                        bulk_copy_g2s(dst + static_cast<size_t>(R) * nc,
+                                      static_cast<const uint4*>(a.residual) + row_off + j0, bytes, &full[s]);
+                }
                 ++it;
                 if (++s == stages) {
                     s = 0;
@@ -233,6 +238,8 @@ k_fused_oneshot_tma(const FusedArgs a, const int stages)
             if (c < nchunk) {
                 if (!gave_up && !mbar_wait_bounded(&full[s], ph))
                     gave_up = true;
+                // The warp gives up as one, so lane 0's release below speaks for it.
+                gave_up = __any_sync(0xffffffffu, gave_up);
                 const int j = c * nc + tid;
                 if (!gave_up && j < a.units_row) {
                     const uint4* src = ring + static_cast<size_t>(s) * slot_vecs + tid;
@@ -258,8 +265,12 @@ k_fused_oneshot_tma(const FusedArgs a, const int stages)
                 }
                 // The warp is done with the slot: its lanes' shared-memory reads
                 // are ordered before lane 0's (releasing) arrival by __syncwarp.
+                // A warp that gave up releases nothing more: the copies of a
+                // stage it did not see complete may still be landing, and the
+                // producer must not re-arm that slot; its own bounded wait for
+                // the release ends its loop instead.
                 __syncwarp();
-                if (lane == 0)
+                if (lane == 0 && !gave_up)
                     mbar_arrive(&empty[s]);
                 if (++s == stages) {
                     s = 0;
