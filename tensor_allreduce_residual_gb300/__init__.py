@@ -124,15 +124,18 @@ def dtype_code(dtype: torch.dtype) -> int:
         raise ValueError(f"unsupported dtype {dtype}; expected float32, float16 or bfloat16") from None
 
 
+_STRATEGY_CODES = {**STRATEGIES, **{k.lower(): v for k, v in STRATEGIES.items()}}
+
+
 def _strategy(s) -> int:
-    return STRATEGIES[s.upper()] if isinstance(s, str) else int(s)
+    if isinstance(s, str):
+        code = _STRATEGY_CODES.get(s)
+        return code if code is not None else STRATEGIES[s.upper()]
+    return int(s)
 
 
 def _ptr_array(ptrs):
-    arr = (ctypes.c_void_p * max(1, len(ptrs)))()
-    for k, p in enumerate(ptrs):
-        arr[k] = p
-    return arr
+    return (ctypes.c_void_p * max(1, len(ptrs)))(*ptrs)
 
 
 def _dev_ptr(t: Optional[torch.Tensor], what: str) -> Optional[int]:
@@ -145,8 +148,16 @@ def _dev_ptr(t: Optional[torch.Tensor], what: str) -> Optional[int]:
     return t.data_ptr()
 
 
+# The raw handle of the current device's current stream, without building a
+# torch.cuda.Stream object (the public route costs a few microseconds a call).
+_raw_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+_get_device = getattr(torch._C, "_cuda_getDevice", None)
+
+
 def _stream_handle(stream) -> Optional[int]:
     if stream is None:
+        if _raw_stream is not None and _get_device is not None:
+            return _raw_stream(_get_device())
         return torch.cuda.current_stream().cuda_stream
     if isinstance(stream, int):
         return stream
@@ -208,8 +219,9 @@ def ar_sum(partials: Sequence[torch.Tensor], out: Optional[torch.Tensor] = None,
     if len(partials) == 0:
         raise ValueError("ar_sum needs at least one partial")
     p0 = partials[0]
+    shape, dt, device = p0.shape, p0.dtype, p0.device
     for k, p in enumerate(partials):
-        if p.shape != p0.shape or p.dtype != p0.dtype or p.device != p0.device:
+        if p.shape != shape or p.dtype != dt or p.device != device:
             raise ValueError(f"partials[{k}] does not match partials[0] in shape, dtype or device")
     if out is None:
         out = torch.empty_like(p0)
@@ -235,14 +247,15 @@ def ar_residual_rmsnorm(partials: Sequence[torch.Tensor], residual: torch.Tensor
     if residual.dim() != 2:
         raise ValueError("residual must be [tokens, hidden]")
     tokens, hidden = residual.shape
+    n, dt = residual.numel(), residual.dtype
     for k, p in enumerate(partials):
-        if p.numel() != residual.numel() or p.dtype != residual.dtype:
+        if p.numel() != n or p.dtype != dt:
             raise ValueError(f"partials[{k}] must match residual in size and dtype")
     if out is None:
         out = torch.empty_like(residual)
     if residual_out is None:
         residual_out = torch.empty_like(residual)
-    code = dtype_code(residual.dtype)
+    code = dtype_code(dt)
     st = _strategy(strategy)
     if intermediate is None and st in (AR_TWOSHOT, AR_AUTO):
         need = ar_workspace_size_rows(len(partials), hidden, tokens, code)
@@ -253,7 +266,7 @@ def ar_residual_rmsnorm(partials: Sequence[torch.Tensor], residual: torch.Tensor
     ptrs = _ptr_array([_dev_ptr(p, f"partials[{k}]") for k, p in enumerate(partials)])
     status = lib().ar_residual_rmsnorm(
         ptrs, len(partials), _dev_ptr(bias, "bias"), _dev_ptr(residual, "residual"),
-        _dev_ptr(weight, "weight"), ctypes.c_float(eps), hidden, tokens, _dev_ptr(out, "out"),
+        _dev_ptr(weight, "weight"), eps, hidden, tokens, _dev_ptr(out, "out"),
         _dev_ptr(residual_out, "residual_out"), ws_ptr, ws_bytes, code, st, _stream_handle(stream))
     _check("ar_residual_rmsnorm", status)
     return out, residual_out
