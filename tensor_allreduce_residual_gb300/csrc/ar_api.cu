@@ -340,20 +340,24 @@ int twoshot_nchunk(int units_row)
 
 size_t round256(size_t b) { return (b + 255) / 256 * 256; }
 
-// Register-resident norm shape: 4 packed vectors per thread for rows of
-// 1024 vectors or more, 8 below (16 elements on the element-wise path), and
-// fewer when a row would get less than a warp; blocks of at least 128
-// threads.  Measured on 8192-row tensors: 46.6 us (8192 bf16, 4 per thread)
-// and 20.8 us (4096 fp16, 8 per thread), 0.85 and 0.95 of the copy peak.
+// Register-resident norm shape: 4 packed vectors per thread for rows of 512
+// to 1024 vectors (8 for longer rows, whose blocks would pass 256 threads),
+// 8 below 512 (16 elements on the element-wise path), and fewer when a row
+// would get less than a warp; blocks of at least 128 threads.  Measured on
+// 8192-row tensors: 42.2 us (8192 bf16) and 20.6 us (4096 fp16), both at 4
+// per thread, 0.94 and 0.96 of the copy peak.
 // `vpt` forces the units per thread (measurement only).  False when the row
 // does not fit one block.
 bool norm_shape(int units_row, bool packed, OneShotShape* sh, int vpt = 0)
 {
     const int max_vpt = packed ? ar::kMaxVPTVec : ar::kMaxVPTScalar;
     if (vpt <= 0) {
-        vpt = packed && units_row >= 1024 ? 4 : max_vpt;
+        vpt = packed && units_row >= 512 ? 4 : max_vpt;
         while (vpt > 1 && (units_row + vpt - 1) / vpt < 32)
             vpt >>= 1;
+        // A row too long for 4 vectors a thread in one block takes 8.
+        if (packed && vpt == 4 && next_pow2((units_row + 3) / 4) > ar::norm_max_threads(true, 4))
+            vpt = 8;
     }
     if (vpt > max_vpt)
         return false;

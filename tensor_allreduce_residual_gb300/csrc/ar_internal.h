@@ -40,10 +40,17 @@ __host__ __device__ constexpr int oneshot_max_threads(int values)
 
 // Largest block of the norm kernel k_rmsnorm for `vpt` units per thread: 8
 // packed vectors (32 registers of row data) need a 512-thread cap to stay
-// out of local memory; everything else fits 1024 threads.
+// out of local memory; 4 packed vectors run in blocks of at most 256
+// threads, norm_min_blocks of them per SM (40 registers a thread, against 60
+// without the hint: 6 rows in flight per SM instead of 4); everything else
+// fits 1024 threads.
 __host__ __device__ constexpr int norm_max_threads(bool packed, int vpt)
 {
-    return packed && vpt >= 8 ? 512 : kMaxTPR;
+    return packed && vpt >= 8 ? 512 : (packed && vpt == 4 ? 256 : kMaxTPR);
+}
+__host__ __device__ constexpr int norm_min_blocks(bool packed, int vpt)
+{
+    return packed && vpt == 4 ? 6 : 1;
 }
 
 struct SumArgs {

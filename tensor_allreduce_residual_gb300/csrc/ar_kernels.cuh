@@ -638,7 +638,7 @@ k_fused_oneshot_persist(const FusedArgs a)
 // x is a.partials[0]; out may alias x.
 // ---------------------------------------------------------------------------
 template <typename T, bool PACKED, int VPT>
-__global__ void __launch_bounds__(norm_max_threads(PACKED, VPT))
+__global__ void __launch_bounds__(norm_max_threads(PACKED, VPT), norm_min_blocks(PACKED, VPT))
 k_rmsnorm(const FusedArgs a, const int tpr)
 {
     pdl_enter();
