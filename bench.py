@@ -381,6 +381,19 @@ def run_extras(ar, torch, workloads, parts, resid, weight, bias, out, res_out, w
             parts, resid, weight, EPS, bias=bias, out=out, residual_out=res_out, intermediate=ws,
             strategy=s), stream, 100)
         ex[f"prefill_{s}"] = {"us_per_call": round(ms * 1e3, 2), "GBps": round(bytes_call / ms / 1e6, 1)}
+    # The Lamport-style call on the same inputs: its buffer is written, read
+    # and emptied again, 3 R n s bytes beyond the fused call's (GBps counts the
+    # fused call's bytes, GBps_protocol all of them).
+    T0, H0 = resid.shape
+    lam = ar.lamport_buffer(len(parts), H0, T0, resid.dtype, resid.device)
+    ms = _time_calls(torch, lambda: ar.ar_residual_rmsnorm_lamport(parts, resid, weight, EPS, bias=bias, out=out,
+                                                                   residual_out=res_out, buffer=lam), stream, 30)
+    extra = 3 * len(parts) * T0 * H0 * resid.element_size()
+    ex["prefill_LAMPORT"] = {"us_per_call": round(ms * 1e3, 2), "GBps": round(bytes_call / ms / 1e6, 1),
+                             "protocol_bytes": bytes_call + extra,
+                             "GBps_protocol": round((bytes_call + extra) / ms / 1e6, 1),
+                             "over_oneshot": round(ms * 1e3 / ex["prefill_ONESHOT"]["us_per_call"], 3)}
+    del lam
     # The unfused route (the pages' "all-reduce, then norm"): ar_sum into a
     # temporary, then the residual + bias + norm call with that sum as its one
     # partial.  It moves (R+1)n s + 4n s + 2H s bytes against the fused
@@ -439,9 +452,13 @@ def run_extras(ar, torch, workloads, parts, resid, weight, bias, out, res_out, w
         o, r = torch.empty_like(f.residual), torch.empty_like(f.residual)
         fn = lambda f=f, o=o, r=r: ar.ar_residual_rmsnorm(f.partials, f.residual, f.weight, f.eps, bias=f.bias,  # noqa: E731
                                                           out=o, residual_out=r, strategy="ONESHOT")
+        lam = ar.lamport_buffer(2, 4096, T, torch.float16)
+        fl = lambda f=f, o=o, r=r, lam=lam: ar.ar_residual_rmsnorm_lamport(  # noqa: E731
+            f.partials, f.residual, f.weight, f.eps, bias=f.bias, out=o, residual_out=r, buffer=lam)
         dec[f"T{T}"] = {"us_warm": round(_time_calls(torch, fn, stream, 200) * 1e3, 2),
                         "us_cold": round(_time_cold(torch, fn, stream, flush, 30) * 1e3, 2),
-                        "us_graph": round(_time_graph(torch, fn) * 1e3, 2)}
+                        "us_graph": round(_time_graph(torch, fn) * 1e3, 2),
+                        "us_graph_lamport": round(_time_graph(torch, fl) * 1e3, 2)}
     ex["tp_decode_R2_fp16_H4096"] = dec
     r8 = {}
     for T in workloads.DECODE_R8_TOKENS:
@@ -452,14 +469,18 @@ def run_extras(ar, torch, workloads, parts, resid, weight, bias, out, res_out, w
                                                                  out=o, residual_out=r, intermediate=w8,
                                                                  strategy="AUTO")
         b = algorithmic_bytes(8, T, 8192, 2, has_bias=False)
-        graph = {}   # the three strategies back to back, before any L2 flush
+        graph = {}   # the three strategies and the Lamport call back to back, before any L2 flush
         for s in ("ONESHOT", "TWOSHOT", "AUTO"):
             graph[s] = _time_graph(torch, lambda f=f, o=o, r=r, w8=w8, s=s: ar.ar_residual_rmsnorm(
                 f.partials, f.residual, f.weight, f.eps, out=o, residual_out=r, intermediate=w8, strategy=s)) * 1e3
+        lam = ar.lamport_buffer(8, 8192, T, torch.bfloat16)
+        graph["LAMPORT"] = _time_graph(torch, lambda f=f, o=o, r=r, lam=lam: ar.ar_residual_rmsnorm_lamport(
+            f.partials, f.residual, f.weight, f.eps, out=o, residual_out=r, buffer=lam)) * 1e3
         cold = _time_cold(torch, fn, stream, flush, 30)
         r8[f"T{T}"] = {"us_warm": round(_time_calls(torch, fn, stream, 100) * 1e3, 2), "us_cold": round(cold * 1e3, 2),
                        "GBps_cold": round(b / cold / 1e6, 1), "us_graph": round(graph["AUTO"], 2),
                        "us_graph_oneshot": round(graph["ONESHOT"], 2), "us_graph_twoshot": round(graph["TWOSHOT"], 2),
+                       "us_graph_lamport": round(graph["LAMPORT"], 2),
                        "us_graph_after_flush": round(_time_graph(torch, fn) * 1e3, 2),
                        "auto": ar.STRATEGY_NAMES[ar.ar_query_strategy(8, T * 8192, 8192, ar.AR_BF16)[0]]}
     for v in r8.values():   # AUTO against the better fixed strategy (graph replay)

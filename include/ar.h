@@ -400,6 +400,98 @@ int ar_residual_rmsnorm_noalloc(const void* const* partials, int R, const void* 
                                 int hidden, int tokens, void* out, void* residual_out,
                                 int dtype, ar_stream_t stream);
 
+/*
+ * Lamport-style fused call (lamport_style_one_shot_all_reduce_norm_kernel
+ * and its launcher, is_lamport_supported and heuristic_min_warp_number,
+ * "allreduce.d2").  The pages name these steps but do not spell them out;
+ * this is the protocol those names stand for, on one GPU:
+ *   - a communication buffer holds one slot per rank, filled beforehand with
+ *     an "empty" marker, the negative zero of the element type;
+ *   - each rank writes its partial into its slot, storing any -0.0 element
+ *     as +0.0 so that no data element equals the marker;
+ *   - the reducer reads each element of every slot until it is no longer
+ *     the marker (the data is its own ready flag: no barrier, no flag
+ *     word), computes the fused op, and writes the marker back, leaving the
+ *     buffer empty for the next call.
+ * Here the R ranks' writes are made by the same kernel launch that reduces
+ * (one cooperative launch: its blocks push first, then reduce rows pushed
+ * by other blocks), so the call reads the R partials like the other fused
+ * calls and returns the same out and residual_out, except that an element
+ * of residual_out or out that is an exact zero may have the other sign.
+ * On one GPU it moves more bytes than the one-shot call (the buffer is
+ * written, read and emptied: 3 * R * tokens * hidden elements more), and
+ * it is provided for the protocol, not for speed.
+ *
+ * Buffer layout: slot r = [tokens][hidden] elements at offset
+ *   r * tokens * hidden * element size; ar_lamport_buffer_size gives the
+ *   bytes.  The buffer is caller-owned device memory, 16-byte aligned, and
+ *   must hold the marker everywhere before a call: fill it once with
+ *   ar_lamport_init; every call that completes leaves it that way.  A buffer
+ *   filled for one element type serves calls of that type only (the fp32
+ *   and 16-bit markers differ).  Calls that share a buffer must be ordered
+ *   (one stream, or events).
+ */
+
+/* Bytes of the Lamport buffer for R partials of [tokens, hidden] elements
+ * (R * tokens * hidden * element size, rounded up to 256); 0 for bad
+ * arguments. */
+size_t ar_lamport_buffer_size(int R, int hidden, int tokens, int dtype);
+
+/*
+ * ar_lamport_init -- fills `bytes` of `buffer` with the empty marker of
+ * `dtype`, asynchronously on `stream`.  buffer: device memory, 16-byte
+ * aligned; bytes: even (0 does nothing).
+ * Errors: AR_ERR_INVALID_ARG (NULL or misaligned buffer, odd bytes),
+ *         AR_ERR_UNSUPPORTED (unknown dtype), AR_ERR_CUDA.
+ */
+int ar_lamport_init(void* buffer, size_t bytes, int dtype, ar_stream_t stream);
+
+/*
+ * ar_lamport_supported -- the is_lamport_supported analogue: AR_OK if the
+ * Lamport call can take this shape, with *warps_per_token (nullable) set to
+ * the warps that reduce one row (the heuristic_min_warp_number analogue).
+ * The shape must have hidden a multiple of 16 / element size and a row that
+ * fits: one block of at most 512 threads (256 when a thread holds more than
+ * 16 values) takes a row, up to 8 16-byte vectors a thread, except that up
+ * to 8 tokens whose R partials hold at least 8192 vectors a row are split
+ * over 4 such blocks.  So rows of up to 2048 vectors (16384 fp16 / bf16,
+ * 8192 fp32 elements) are always taken, and up to 4 times longer ones in
+ * that split case.
+ * Host-side only: launches nothing.  Pointer alignment is checked by the
+ * call itself.
+ * Errors: AR_ERR_INVALID_ARG (bad R, hidden or tokens),
+ *         AR_ERR_UNSUPPORTED (unknown dtype, or a shape the call cannot take).
+ */
+int ar_lamport_supported(int R, int hidden, int tokens, int dtype, int* warps_per_token);
+
+/*
+ * ar_residual_rmsnorm_lamport -- the fused op of ar_residual_rmsnorm (same
+ * arguments with the same meaning and layout; no strategy, and the
+ * Lamport buffer in place of the two-shot workspace) through the Lamport
+ * protocol.
+ *   lamport_buffer  device buffer of at least ar_lamport_buffer_size(R,
+ *                   hidden, tokens, dtype) bytes, 16-byte aligned, filled
+ *                   with the marker (ar_lamport_init) and left so on return.
+ * Aliasing: residual_out may be residual and out may be a partial (each
+ *   partial element is pushed before anything that depends on it is
+ *   written); the buffer may not overlap any other argument.
+ * Requirements: every tensor pointer 16-byte aligned and hidden a multiple
+ *   of 16 / element size (the 16-byte packed path); otherwise
+ *   AR_ERR_UNSUPPORTED.
+ * Waits: each poll of an element gives up after one second; the kernel then
+ *   finishes without hanging, its outputs are incomplete, the event is
+ *   recorded for ar_device_status (AR_ERR_TIMEOUT), and the buffer must be
+ *   filled again with ar_lamport_init before it is used again.
+ * Errors: those of ar_residual_rmsnorm, plus AR_ERR_WORKSPACE for a NULL,
+ *   misaligned or too small buffer; AR_ERR_UNSUPPORTED as above, or if the
+ *   device cannot make the launch cooperative.
+ */
+int ar_residual_rmsnorm_lamport(const void* const* partials, int R, const void* bias,
+                                const void* residual, const void* weight, float eps,
+                                int hidden, int tokens, void* out, void* residual_out,
+                                void* lamport_buffer, size_t lamport_bytes, int dtype,
+                                ar_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -111,6 +111,12 @@ def lib() -> ctypes.CDLL:
     L.ar_residual_rmsnorm_host.restype = i
     L.ar_query_launch.argtypes = [i, i, i, i, i, ctypes.POINTER(ArLaunchPlan)]
     L.ar_query_launch.restype = i
+    L.ar_lamport_buffer_size.argtypes, L.ar_lamport_buffer_size.restype = [i, i, i, i], sz
+    L.ar_lamport_init.argtypes, L.ar_lamport_init.restype = [vp, sz, i, vp], i
+    L.ar_lamport_supported.argtypes = [i, i, i, i, ctypes.POINTER(i)]
+    L.ar_lamport_supported.restype = i
+    L.ar_residual_rmsnorm_lamport.argtypes = [pvp, i, vp, vp, vp, ctypes.c_float, i, i, vp, vp, vp, sz, i, vp]
+    L.ar_residual_rmsnorm_lamport.restype = i
     _lib = L
     return L
 
@@ -122,6 +128,11 @@ def dtype_code(dtype: torch.dtype) -> int:
         return _TORCH_TO_AR[dtype]
     except KeyError:
         raise ValueError(f"unsupported dtype {dtype}; expected float32, float16 or bfloat16") from None
+
+
+def _code(dtype) -> int:
+    """An ar_dtype code, given as one or as a torch dtype."""
+    return dtype if isinstance(dtype, int) else dtype_code(dtype)
 
 
 _STRATEGY_CODES = {**STRATEGIES, **{k.lower(): v for k, v in STRATEGIES.items()}}
@@ -387,3 +398,67 @@ def make_params(partials, out, *, bias=None, residual=None, weight=None, eps=0.0
     p.workspace = _dev_ptr(workspace, "workspace")
     p.workspace_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     return p
+
+
+def ar_lamport_buffer_size(R: int, hidden: int, tokens: int, dtype) -> int:
+    """Bytes of the Lamport buffer for R partials of [tokens, hidden] (0 for bad arguments)."""
+    return int(lib().ar_lamport_buffer_size(R, hidden, tokens, _code(dtype)))
+
+
+def ar_lamport_init(buffer: torch.Tensor, dtype, stream=None) -> torch.Tensor:
+    """Fills the whole CUDA tensor ``buffer`` with the empty marker of ``dtype`` (negative zero)."""
+    nbytes = buffer.numel() * buffer.element_size()
+    _check("ar_lamport_init", lib().ar_lamport_init(_dev_ptr(buffer, "buffer"), nbytes, _code(dtype),
+                                                    _stream_handle(stream)))
+    return buffer
+
+
+def ar_lamport_supported(R: int, hidden: int, tokens: int, dtype) -> Optional[int]:
+    """Warps per row of the Lamport call for this shape, or None if it cannot take the shape."""
+    w = ctypes.c_int(0)
+    status = lib().ar_lamport_supported(R, hidden, tokens, _code(dtype), ctypes.byref(w))
+    if status == AR_ERR_UNSUPPORTED:
+        return None
+    _check("ar_lamport_supported", status)
+    return w.value
+
+
+def lamport_buffer(R: int, hidden: int, tokens: int, dtype: torch.dtype, device=None) -> torch.Tensor:
+    """A new device buffer for ar_residual_rmsnorm_lamport, filled with the empty marker."""
+    nbytes = ar_lamport_buffer_size(R, hidden, tokens, dtype)
+    if nbytes == 0:
+        raise ValueError("no Lamport buffer for this shape")
+    buf = torch.empty(nbytes, dtype=torch.uint8, device=device if device is not None else "cuda")
+    return ar_lamport_init(buf, dtype)
+
+
+def ar_residual_rmsnorm_lamport(partials: Sequence[torch.Tensor], residual: torch.Tensor, weight: torch.Tensor,
+                                eps: float, bias: Optional[torch.Tensor] = None,
+                                out: Optional[torch.Tensor] = None, residual_out: Optional[torch.Tensor] = None,
+                                buffer: Optional[torch.Tensor] = None, stream=None):
+    """(out, residual_out) of the fused op through the Lamport protocol.
+
+    ``buffer`` is the marker-filled Lamport buffer (see lamport_buffer); every
+    completed call leaves it filled again, so one buffer serves a sequence of
+    calls on one stream.  When it is None a new one is made for this call.
+    """
+    if residual.dim() != 2:
+        raise ValueError("residual must be [tokens, hidden]")
+    tokens, hidden = residual.shape
+    for k, p in enumerate(partials):
+        if p.numel() != residual.numel() or p.dtype != residual.dtype:
+            raise ValueError(f"partials[{k}] must match residual in size and dtype")
+    if out is None:
+        out = torch.empty_like(residual)
+    if residual_out is None:
+        residual_out = torch.empty_like(residual)
+    if buffer is None:
+        buffer = lamport_buffer(len(partials), hidden, tokens, residual.dtype, residual.device)
+    ptrs = _ptr_array([_dev_ptr(p, f"partials[{k}]") for k, p in enumerate(partials)])
+    status = lib().ar_residual_rmsnorm_lamport(
+        ptrs, len(partials), _dev_ptr(bias, "bias"), _dev_ptr(residual, "residual"),
+        _dev_ptr(weight, "weight"), ctypes.c_float(eps), hidden, tokens, _dev_ptr(out, "out"),
+        _dev_ptr(residual_out, "residual_out"), _dev_ptr(buffer, "buffer"),
+        buffer.numel() * buffer.element_size(), dtype_code(residual.dtype), _stream_handle(stream))
+    _check("ar_residual_rmsnorm_lamport", status)
+    return out, residual_out

@@ -18,7 +18,7 @@ BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libar.so")
 
 SOURCES = ["ar_api.cu", "ar_kern_f32.cu", "ar_kern_f16.cu", "ar_kern_bf16.cu", "ar_noalloc.cu", "ar_host.cu"]
-HEADERS = ["ar_internal.h", "ar_kernels.cuh", "ar_tma.cuh", "ar_launch.cuh", "ar_auto_table.h"]
+HEADERS = ["ar_internal.h", "ar_kernels.cuh", "ar_tma.cuh", "ar_lamport.cuh", "ar_launch.cuh", "ar_auto_table.h"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",

@@ -372,6 +372,70 @@ bool norm_shape(int units_row, bool packed, OneShotShape* sh, int vpt = 0)
     return true;
 }
 
+// Lamport-style call.  Up to 8 rows whose R partials hold at least 8192
+// 16-byte vectors: each row split over 4 blocks, with the smallest units per
+// thread that fit lamport_max_threads (R=8 bf16 rows of 8192: 6.5 us at one
+// token against 7.4 us unsplit; splitting over 8 blocks, or splitting
+// shorter rows, measured slower: the exchange of the partial sums of squares
+// costs about as much as it saves).  Otherwise the register-resident
+// one-shot shape (heuristic_min_warp_number: threads per row from the
+// one-shot rule), its blocks capped at lamport_max_threads.  The shape
+// override forces either: mode kRegisters with its units per thread, or
+// mode kCluster with its units per thread and split (measurement only).
+int lamport_split_rule(int tokens, int R, int units_row)
+{
+    return tokens <= 8 && static_cast<long long>(R) * units_row >= 8192 ? 4 : 1;
+}
+
+bool lamport_shape(int units_row, int tokens, int lanes, int R, OneShotShape* sh)
+{
+    auto fits = [&](int vpt) {
+        return oneshot_shape(units_row, vpt, lanes, true, ar::kRegisters, R, sh) &&
+               sh->tpr * sh->rows <= ar::lamport_max_threads(vpt * lanes);
+    };
+    auto fits_split = [&](int vpt, int c) {
+        return static_cast<long long>(tokens) * c <= INT32_MAX && cluster_shape(units_row, vpt, lanes, c, sh) &&
+               sh->tpr <= ar::lamport_max_threads(vpt * lanes);
+    };
+    const ShapeOverride& ov = shape_override();
+    if (ov.vpt > 0 && ov.mode == ar::kRegisters && fits(ov.vpt))
+        return true;
+    if (ov.vpt > 0 && ov.mode == ar::kCluster && fits_split(ov.vpt, ov.blocks_per_sm))
+        return true;
+    int c = lamport_split_rule(tokens, R, units_row);
+    while (c > 1 && (units_row + c - 1) / c < 32)  // no slice shorter than a warp
+        c >>= 1;
+    if (c > 1)
+        for (int vpt = 1; vpt <= ar::kMaxVPTVec; vpt <<= 1)
+            if (fits_split(vpt, c))
+                return true;
+    for (int vpt = rule_vpt(units_row, tokens, lanes, true); vpt <= ar::kMaxVPTVec; vpt <<= 1)
+        if (fits(vpt))
+            return true;
+    return false;
+}
+
+// Bytes of the Lamport buffer: the R slots, then the exchange area.
+size_t lamport_buffer_bytes(int R, int hidden, int tokens, int esize)
+{
+    return static_cast<size_t>(R) * tokens * hidden * esize +
+           static_cast<size_t>(tokens) * ar::kLamportRowWords * sizeof(uint32_t);
+}
+
+// Test-only fault injection for the Lamport call's bounded waits:
+// AR_TEST_LAMPORT_SKIP_RANK=r leaves rank r's pushes out, so the polls of
+// its slot run out (about a second); ar_device_status then reports
+// AR_ERR_TIMEOUT.  Read once per process; unset means -1 (none).
+int test_lamport_skip_rank()
+{
+    static const int v = [] {
+        const char* e = std::getenv("AR_TEST_LAMPORT_SKIP_RANK");
+        const int r = e != nullptr ? std::atoi(e) : -1;
+        return r >= 0 && r < AR_MAX_RANKS ? r : -1;
+    }();
+    return v;
+}
+
 }  // namespace
 
 extern "C" {
@@ -766,6 +830,106 @@ int ar_query_strategy(int R, size_t n, int hidden, int dtype, int fusion_op, int
     if (warps_per_token)
         *warps_per_token = plan.strategy == AR_ONESHOT ? (row_threads + 31) / 32 : 0;
     return AR_OK;
+}
+
+size_t ar_lamport_buffer_size(int R, int hidden, int tokens, int dtype)
+{
+    const int esize = esize_of(dtype);
+    if (R < 1 || R > AR_MAX_RANKS || hidden < 1 || tokens < 0 || esize == 0)
+        return 0;
+    return round256(lamport_buffer_bytes(R, hidden, tokens, esize));
+}
+
+int ar_lamport_init(void* buffer, size_t bytes, int dtype, ar_stream_t stream)
+{
+    if (esize_of(dtype) == 0)
+        return AR_ERR_UNSUPPORTED;
+    if (buffer == nullptr || !aligned16(buffer) || bytes % 2 != 0)
+        return AR_ERR_INVALID_ARG;
+    if (bytes == 0)
+        return AR_OK;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    return status_of(by_dtype(dtype, [&](auto tag) {
+        using T = decltype(tag);
+        return ar::launch_lamport_fill<T>(buffer, bytes, s);
+    }));
+}
+
+int ar_lamport_supported(int R, int hidden, int tokens, int dtype, int* warps_per_token)
+{
+    if (R < 1 || R > AR_MAX_RANKS || hidden < 1 || tokens < 0)
+        return AR_ERR_INVALID_ARG;
+    const int esize = esize_of(dtype);
+    if (esize == 0)
+        return AR_ERR_UNSUPPORTED;
+    const int lanes = 16 / esize;
+    OneShotShape sh{};
+    if (hidden % lanes != 0 || !lamport_shape(hidden / lanes, tokens, lanes, R, &sh))
+        return AR_ERR_UNSUPPORTED;
+    if (warps_per_token)
+        *warps_per_token = (sh.tpr * (sh.mode == ar::kCluster ? sh.cluster : 1) + 31) / 32;
+    return AR_OK;
+}
+
+int ar_residual_rmsnorm_lamport(const void* const* partials, int R, const void* bias, const void* residual,
+                                const void* weight, float eps, int hidden, int tokens, void* out,
+                                void* residual_out, void* lamport_buffer, size_t lamport_bytes, int dtype,
+                                ar_stream_t stream)
+{
+    if (R < 1 || R > AR_MAX_RANKS || hidden < 1 || tokens < 0)
+        return AR_ERR_INVALID_ARG;
+    const int esize = esize_of(dtype);
+    if (esize == 0)
+        return AR_ERR_UNSUPPORTED;
+    if (!std::isfinite(eps) || eps < 0.0f)
+        return AR_ERR_INVALID_ARG;
+    if (tokens == 0)
+        return AR_OK;
+    if (partials == nullptr || residual == nullptr || weight == nullptr || out == nullptr ||
+        residual_out == nullptr || out == residual_out)
+        return AR_ERR_INVALID_ARG;
+    for (int r = 0; r < R; ++r)
+        if (partials[r] == nullptr)
+            return AR_ERR_INVALID_ARG;
+    const int lanes = 16 / esize;
+    bool packed = hidden % lanes == 0 && aligned16(residual) && aligned16(weight) && aligned16(out) &&
+                  aligned16(residual_out) && (bias == nullptr || aligned16(bias));
+    for (int r = 0; r < R; ++r)
+        packed = packed && aligned16(partials[r]);
+    if (!packed)
+        return AR_ERR_UNSUPPORTED;
+    const int units_row = hidden / lanes;
+    OneShotShape sh{};
+    if (!lamport_shape(units_row, tokens, lanes, R, &sh))
+        return AR_ERR_UNSUPPORTED;
+    const size_t need = lamport_buffer_bytes(R, hidden, tokens, esize);
+    if (lamport_buffer == nullptr || !aligned16(lamport_buffer) || lamport_bytes < need)
+        return AR_ERR_WORKSPACE;
+
+    FusedArgs a{};
+    for (int r = 0; r < R; ++r)
+        a.partials[r] = partials[r];
+    a.bias = bias;
+    a.residual = residual;
+    a.weight = weight;
+    a.out = out;
+    a.residual_out = residual_out;
+    a.R = R;
+    a.hidden = hidden;
+    a.tokens = tokens;
+    a.units_row = units_row;
+    a.eps = eps;
+    a.early_residual = 1;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const int skip = test_lamport_skip_rank();
+    const cudaError_t e = by_dtype(dtype, [&](auto tag) {
+        using T = decltype(tag);
+        return ar::launch_fused_lamport<T>(a, lamport_buffer, sh, skip < R ? skip : -1, s);
+    });
+    if (e == cudaErrorInvalidConfiguration || e == cudaErrorCooperativeLaunchTooLarge ||
+        e == cudaErrorNotSupported)
+        return AR_ERR_UNSUPPORTED;
+    return status_of(e);
 }
 
 }  // extern "C"

@@ -38,6 +38,14 @@ __host__ __device__ constexpr int oneshot_max_threads(int values)
     return values <= 16 ? 1024 : (values <= 32 ? 512 : 256);
 }
 
+// Largest block of the Lamport-style fused kernel for a thread that holds
+// `values` fp32 values of its row: half the one-shot kernel's, because it
+// also holds the R slot vectors of the unit it is polling.
+__host__ __device__ constexpr int lamport_max_threads(int values)
+{
+    return values <= 16 ? 512 : 256;
+}
+
 // Largest block of the norm kernel k_rmsnorm for `vpt` units per thread: 8
 // packed vectors (32 registers of row data) need a 512-thread cap to stay
 // out of local memory; 4 packed vectors run in blocks of at most 256
@@ -160,6 +168,24 @@ cudaError_t launch_rmsnorm(const FusedArgs& a, bool packed, OneShotShape shape, 
 // a.partials[0] is x, a.R == 1, no bias, residual or residual_out.
 template <typename T>
 cudaError_t launch_rmsnorm_tma(const FusedArgs& a, OneShotShape shape, cudaStream_t s);
+
+// Lamport-style fused call.  Buffer: R slots of tokens * units_row 16-byte
+// vectors, then an exchange area of kLamportRowWords 32-bit words per row for
+// rows split over up to kLamportMaxSplit blocks.
+constexpr int kLamportMaxSplit = 8;
+constexpr int kLamportRowWords = 16;
+
+// Pushes the R partials into the marker-filled buffer `lam`, then reduces
+// from it in the same cooperative launch.  shape.mode == kRegisters: tpr
+// threads a row; shape.mode == kCluster: each row split over shape.cluster
+// blocks of shape.tpr threads.  skip_rank >= 0 leaves that rank's pushes out
+// (tests).
+template <typename T>
+cudaError_t launch_fused_lamport(const FusedArgs& a, void* lam, OneShotShape shape, int skip_rank, cudaStream_t s);
+
+// Fills `bytes` of `buf` (16-byte aligned, bytes even) with T's empty marker.
+template <typename T>
+cudaError_t launch_lamport_fill(void* buf, size_t bytes, cudaStream_t s);
 
 // Number of bounded waits that gave up in the kernels of element type T since
 // the last call, which resets it.  Synchronous (reads device memory).

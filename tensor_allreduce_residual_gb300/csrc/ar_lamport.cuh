@@ -1,0 +1,375 @@
+// ar_lamport.cuh -- the Lamport-style one-shot fused sum + bias + residual +
+// RMSNorm (lamport_style_one_shot_all_reduce_norm_kernel_launcher ->
+// lamport_style_one_shot_all_reduce_norm_kernel, "allreduce.d2"), for one
+// GPU, sm_103a.
+//
+// The protocol.  Every rank writes its partial into a communication buffer
+// that holds an "empty" marker wherever nothing has been written yet: the
+// negative zero of the element type, a value the writers never store (a
+// -0.0 lane of a partial is written as +0.0, the same number in every sum
+// here; only the sign of an exact-zero result can change).  The reducer
+// needs no barrier and no flag: it re-reads an element of the buffer until
+// it is not the marker, which proves that this element has arrived, and once
+// it has used the element it writes the marker back, so the buffer is empty
+// again for the next call.  The data is its own ready flag.
+//
+// On one GPU the R ranks' writes are emulated inside the same launch.  The
+// buffer holds one slot per rank, slot r = [tokens][units_row] 16-byte
+// vectors at r * tokens * units_row.  Every block first pushes its
+// grid-stride share of (row, unit) vectors of all R partials into their
+// slots (the peers' NVLink writes of the multi-GPU protocol), then reduces
+// its rows as the register-resident one-shot kernel does -- tpr threads per
+// row, VPT vectors per thread, fp32 sums in rank order, bias, residual, the
+// row's sum of squares over a fixed tree -- reading each partial from its
+// slot instead of from the partial.  The rows a block reduces were pushed
+// by other blocks, so blocks wait on one another: the launch is cooperative
+// (all of its blocks resident at once, or the launch fails), so every push
+// it waits for is made by a block that is already running.
+//
+// Memory ordering.  Pushes are st.relaxed.gpu and polls ld.relaxed.gpu, both
+// of 16 bytes: each 2- or 4-byte element is written once, from the marker to
+// its value, and read until it is no longer the marker, so a vector read
+// part-way through a push shows some elements still empty and is read
+// again.  No fence is needed: nothing but the element itself is published.
+// The marker is written back with a plain store by the one thread that read
+// the element; the next call's pushes are ordered after it by the kernel
+// boundary.
+//
+// Waits are bounded: a poll that has not seen its element after
+// kWaitLimitNs gives up, counts the event in g_wait_timeouts (read by the
+// host through take_wait_timeouts) and the thread polls no more in this
+// launch; its outputs are then incomplete, and the buffer may hold elements
+// pushed after the give-up, so it has to be emptied again (filled with the
+// marker) before the next call.
+#pragma once
+
+#include "ar_tma.cuh"
+
+namespace ar {
+
+// The empty marker, as the 32-bit word of two 16-bit lanes or one fp32 lane.
+template <typename T>
+struct LamportMarker {
+    static constexpr uint32_t word = 0x80008000u;  // -0.0 in both halves (fp16, bf16)
+};
+template <>
+struct LamportMarker<float> {
+    static constexpr uint32_t word = 0x80000000u;  // -0.0f
+};
+
+__device__ __forceinline__ uint4 ld_relaxed16(const void* p)
+{
+    uint4 r;
+    asm volatile("ld.relaxed.gpu.global.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+                 : "l"(p));
+    return r;
+}
+
+__device__ __forceinline__ void st_relaxed16(void* p, uint4 v)
+{
+    asm volatile("st.relaxed.gpu.global.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z),
+                 "r"(v.w)
+                 : "memory");
+}
+
+// Per 32-bit word: all-ones in each lane equal to the marker, zero elsewhere.
+template <typename T>
+__device__ __forceinline__ uint32_t marker_lanes(uint32_t w)
+{
+    if constexpr (sizeof(T) == 4)
+        return w == LamportMarker<T>::word ? 0xffffffffu : 0u;
+    else
+        return __vcmpeq2(w, LamportMarker<T>::word);
+}
+
+// True if any lane of the vector still holds the marker (not yet pushed).
+template <typename T>
+__device__ __forceinline__ bool lamport_pending(const uint4& v)
+{
+    return (marker_lanes<T>(v.x) | marker_lanes<T>(v.y) | marker_lanes<T>(v.z) | marker_lanes<T>(v.w)) != 0u;
+}
+
+// The vector as a writer pushes it: every -0.0 lane becomes +0.0 (clearing
+// the sign bit of a lane equal to the marker leaves all-zero bits).
+template <typename T>
+__device__ __forceinline__ uint4 lamport_clean(uint4 v)
+{
+    v.x &= ~marker_lanes<T>(v.x);
+    v.y &= ~marker_lanes<T>(v.y);
+    v.z &= ~marker_lanes<T>(v.z);
+    v.w &= ~marker_lanes<T>(v.w);
+    return v;
+}
+
+template <typename T>
+__device__ __forceinline__ uint4 lamport_empty()
+{
+    constexpr uint32_t m = LamportMarker<T>::word;
+    return make_uint4(m, m, m, m);
+}
+
+// Re-reads *p until no lane is the marker; `v` is a first read of it.
+// Bounded: after kWaitLimitNs the thread gives up (and polls no more).
+template <typename T>
+__device__ __forceinline__ uint4 lamport_poll(const uint4* p, uint4 v, bool& gave_up)
+{
+    if (!lamport_pending<T>(v) || gave_up)
+        return v;
+    const unsigned long long t0 = global_ns();
+    do {
+        __nanosleep(32);
+        v = ld_relaxed16(p);
+        if (!lamport_pending<T>(v))
+            return v;
+    } while (global_ns() - t0 <= kWaitLimitNs);
+    gave_up = true;
+    atomicAdd(&g_wait_timeouts, 1u);
+    return v;
+}
+
+// x = slot 0 + ... + slot R-1 of vector i in fp32, rank order, each read
+// once it has arrived and then emptied again.  All R first reads are issued
+// before any is checked, so R loads are in flight at once.
+template <typename T, int R_CT>
+__device__ __forceinline__ void lamport_take(uint4* lam, uint64_t slot_units, int R, uint64_t i, float* x,
+                                             bool& gave_up)
+{
+    constexpr int L = Lanes<T>::V;
+    if constexpr (R_CT > 0) {
+        uint4 v[R_CT];
+#pragma unroll
+        for (int r = 0; r < R_CT; ++r)
+            v[r] = ld_relaxed16(lam + r * slot_units + i);
+#pragma unroll
+        for (int r = 0; r < R_CT; ++r)
+            v[r] = lamport_poll<T>(lam + r * slot_units + i, v[r], gave_up);
+#pragma unroll
+        for (int r = 0; r < R_CT; ++r)
+            st16(lam + r * slot_units + i, lamport_empty<T>());
+        Lanes<T>::unpack(v[0], x);
+#pragma unroll
+        for (int r = 1; r < R_CT; ++r) {
+            float t[L];
+            Lanes<T>::unpack(v[r], t);
+            add_lanes<L>(x, t);
+        }
+    } else {
+        for (int r = 0; r < R; ++r) {
+            uint4* p = lam + r * slot_units + i;
+            const uint4 v = lamport_poll<T>(p, ld_relaxed16(p), gave_up);
+            st16(p, lamport_empty<T>());
+            float t[L];
+            Lanes<T>::unpack(v, t);
+            if (r == 0) {
+#pragma unroll
+                for (int l = 0; l < L; ++l)
+                    x[l] = t[l];
+            } else {
+                add_lanes<L>(x, t);
+            }
+        }
+    }
+}
+
+__device__ __forceinline__ uint32_t ld_relaxed32(const uint32_t* p)
+{
+    uint32_t v;
+    asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ void st_relaxed32(uint32_t* p, uint32_t v)
+{
+    asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// The exchange area (kLamportRowWords words per row after the R slots) of a
+// row split over csize blocks: word c holds block c's partial sum of squares
+// and word kLamportMaxSplit counts the blocks that have read all of them;
+// both start as the marker word.
+//
+// Block c's share of a split row's sum of squares in, the row's total out
+// (added in block order, so every block of the row gets the same value).
+// Called by the 32 lanes of one warp, all holding the same share; lane k
+// waits for share k, so the csize waits overlap.  A share is never the
+// marker: it is a sum of squares that starts at +0.0 (>= +0.0 or NaN),
+// while the marker word is -0.0f (fp32) or a negative fp32 bit pattern
+// (16-bit types).  The last of the csize blocks to count itself writes the
+// marker back over the shares and the counter: its acquire-release add
+// orders those stores after every other block's reads, which precede that
+// block's own (release) add.
+template <typename T>
+__device__ __forceinline__ float lamport_exchange(uint32_t* xr, int c, int csize, float share, bool& gave_up)
+{
+    constexpr uint32_t m = LamportMarker<T>::word;
+    const int lane = static_cast<int>(threadIdx.x & 31u);
+    if (lane == c)
+        st_relaxed32(xr + c, __float_as_uint(share));
+    uint32_t v = m;
+    if (lane < csize) {
+        v = ld_relaxed32(xr + lane);
+        if (v == m && !gave_up) {
+            const unsigned long long t0 = global_ns();
+            do {
+                __nanosleep(32);
+                v = ld_relaxed32(xr + lane);
+            } while (v == m && global_ns() - t0 <= kWaitLimitNs);
+            if (v == m) {
+                gave_up = true;
+                atomicAdd(&g_wait_timeouts, 1u);
+            }
+        }
+    }
+    float tot = 0.0f;
+    for (int k = 0; k < csize; ++k) {
+        const uint32_t vk = __shfl_sync(0xffffffffu, v, k);
+        tot += vk == m ? 0.0f : __uint_as_float(vk);
+    }
+    __syncwarp();  // the lanes' reads are ordered before lane 0's add
+    if (lane == 0) {
+        uint32_t before;
+        asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;"
+                     : "=r"(before)
+                     : "l"(xr + kLamportMaxSplit)
+                     : "memory");
+        if (before == m + static_cast<uint32_t>(csize) - 1u) {
+            for (int k = 0; k < csize; ++k)
+                xr[k] = m;
+            xr[kLamportMaxSplit] = m;
+        }
+    }
+    return tot;
+}
+
+// The fused kernel.  Packed path only (16-byte vectors).  csize == 1: tpr
+// threads own a row, blockDim.x / tpr rows per block.  csize > 1: a row is
+// split over csize blocks (consecutive groups), block c owning the
+// contiguous slice [c*S, (c+1)*S) of its vectors (S = ceil(units_row /
+// csize)) with all blockDim.x == tpr threads; the slices' sums of squares
+// meet in the exchange area through the same protocol as the data.
+// `skip_rank` >= 0 leaves that rank's pushes out (tests of the bounded waits
+// only; -1 = none).
+template <typename T, int R_CT, int VPT>
+__global__ void __launch_bounds__(lamport_max_threads(VPT * Lanes<T>::V))
+k_fused_lamport(const FusedArgs a, uint4* lam, const int tpr, const int csize, const int skip_rank)
+{
+    pdl_enter();
+    using U = Unit<T, true>;
+    constexpr int L = U::L;
+    __shared__ float red[2][32];
+    __shared__ float tot_s[2];
+    const int R = R_CT > 0 ? R_CT : a.R;
+    const uint64_t slot_units = static_cast<uint64_t>(a.tokens) * a.units_row;
+
+    // Push: vector i of every partial into its rank's slot.
+    const uint64_t stride = static_cast<uint64_t>(gridDim.x) * blockDim.x;
+    for (uint64_t i = static_cast<uint64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < slot_units; i += stride) {
+        if constexpr (R_CT > 0) {
+            uint4 v[R_CT];
+#pragma unroll
+            for (int r = 0; r < R_CT; ++r)
+                v[r] = ld_stream16(static_cast<const uint4*>(a.partials[r]) + i);
+#pragma unroll
+            for (int r = 0; r < R_CT; ++r)
+                if (r != skip_rank)
+                    st_relaxed16(lam + r * slot_units + i, lamport_clean<T>(v[r]));
+        } else {
+            for (int r = 0; r < R; ++r) {
+                const uint4 v = ld_stream16(static_cast<const uint4*>(a.partials[r]) + i);
+                if (r != skip_rank)
+                    st_relaxed16(lam + r * slot_units + i, lamport_clean<T>(v));
+            }
+        }
+    }
+
+    // Reduce: blocks stride over groups (csize == 1: blockDim.x / tpr rows;
+    // csize > 1: one slice of one row).
+    const bool split = csize > 1;
+    const int rows = split ? 1 : static_cast<int>(blockDim.x) / tpr;
+    const int lane = split ? static_cast<int>(threadIdx.x) : static_cast<int>(threadIdx.x & (tpr - 1));
+    const int row_in_block = split ? 0 : static_cast<int>(threadIdx.x) / tpr;
+    const int slice = split ? (a.units_row + csize - 1) / csize : a.units_row;
+    const int groups = split ? a.tokens * csize : (a.tokens + rows - 1) / rows;
+    uint32_t* xarea = reinterpret_cast<uint32_t*>(lam + static_cast<uint64_t>(R) * slot_units);
+    bool gave_up = false;
+    int parity = 0;
+    for (int g = blockIdx.x; g < groups; g += gridDim.x, parity ^= 1) {
+        const int row = split ? g / csize : g * rows + row_in_block;
+        const int c = split ? g % csize : 0;
+        const int j_begin = c * slice;
+        const int j_end = min(j_begin + slice, a.units_row);
+        const bool row_ok = row < a.tokens;
+        const uint64_t row_off = static_cast<uint64_t>(row) * a.units_row;
+        float x[VPT][L];
+        uint4 wv[VPT];
+        float ss = 0.0f;
+#pragma unroll
+        for (int k = 0; k < VPT; ++k) {
+            const int j = j_begin + lane + k * tpr;
+#pragma unroll
+            for (int l = 0; l < L; ++l)
+                x[k][l] = 0.0f;
+            if (row_ok && j < j_end) {
+                lamport_take<T, R_CT>(lam, slot_units, R, row_off + j, x[k], gave_up);
+                float t[L];
+                if (a.bias != nullptr) {
+                    U::to_float(U::load_cached(a.bias, j), t);
+                    add_lanes<L>(x[k], t);
+                }
+                U::to_float(U::load(a.residual, row_off + j), t);
+                add_lanes<L>(x[k], t);
+                wv[k] = U::load_cached(a.weight, j);
+                U::store(a.residual_out, row_off + j, x[k]);
+#pragma unroll
+                for (int l = 0; l < L; ++l)
+                    ss = fmaf(x[k][l], x[k][l], ss);
+            }
+        }
+        // Double-buffered scratch: a warp that runs ahead into the next
+        // group writes the other half.
+        ss = row_sum(ss, tpr, red[parity]);
+        if (split) {
+            if (threadIdx.x < 32) {
+                const float tot = lamport_exchange<T>(xarea + static_cast<uint64_t>(row) * kLamportRowWords, c,
+                                                      csize, ss, gave_up);
+                if (threadIdx.x == 0)
+                    tot_s[parity] = tot;
+            }
+            __syncthreads();
+            ss = tot_s[parity];
+        }
+        const float inv = inv_rms(ss, a.hidden, a.eps);
+#pragma unroll
+        for (int k = 0; k < VPT; ++k) {
+            const int j = j_begin + lane + k * tpr;
+            if (row_ok && j < j_end) {
+                float w[L], y[L];
+                U::to_float(wv[k], w);
+#pragma unroll
+                for (int l = 0; l < L; ++l)
+                    y[l] = x[k][l] * inv * w[l];
+                U::store(a.out, row_off + j, y);
+            }
+        }
+    }
+}
+
+// Fills `nvec` 16-byte vectors, then `tail_halves` 2-byte halves, with the
+// empty marker of T.
+template <typename T>
+__global__ void __launch_bounds__(kFlatThreads) k_lamport_fill(uint4* buf, uint64_t nvec, uint32_t tail_halves)
+{
+    pdl_enter();
+    const uint64_t stride = static_cast<uint64_t>(gridDim.x) * blockDim.x;
+    for (uint64_t i = static_cast<uint64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < nvec; i += stride)
+        st16(buf + i, lamport_empty<T>());
+    if (blockIdx.x == 0 && threadIdx.x < tail_halves) {
+        // Little-endian halves of the marker word: (low, high).
+        const uint32_t m = LamportMarker<T>::word;
+        const unsigned short half = static_cast<unsigned short>((threadIdx.x & 1u) ? (m >> 16) : (m & 0xffffu));
+        reinterpret_cast<unsigned short*>(buf + nvec)[threadIdx.x] = half;
+    }
+}
+
+}  // namespace ar

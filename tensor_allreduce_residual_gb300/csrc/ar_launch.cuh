@@ -14,6 +14,7 @@
 #include <utility>
 
 #include "ar_kernels.cuh"
+#include "ar_lamport.cuh"
 #include "ar_tma.cuh"
 
 namespace ar {
@@ -313,6 +314,87 @@ cudaError_t launch_fused_twoshot(const FusedArgs& a, bool packed, cudaStream_t s
     }
 }
 
+// Lamport-style fused kernel: one cooperative launch (all blocks resident at
+// once, which its blocks' waits on one another need).  The grid covers the
+// larger of the row groups (rows, or row slices when rows are split) and one
+// pushed vector per thread, capped at the blocks that fit on the device at
+// once; blocks stride over what is left.
+template <typename T, int R_CT, int VPT>
+static cudaError_t run_lamport(const FusedArgs& a, void* lam, OneShotShape sh, int skip_rank, cudaStream_t s)
+{
+    auto kernel = k_fused_lamport<T, R_CT, VPT>;
+    const int threads = sh.tpr * sh.rows;
+    int dev = 0, sms = 0, per_sm = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess)
+        e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e == cudaSuccess)
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads, 0);
+    if (e != cudaSuccess)
+        return e;
+    if (per_sm < 1)
+        return cudaErrorInvalidConfiguration;
+    const int csize = sh.mode == kCluster ? sh.cluster : 1;
+    const long long groups = csize > 1 ? static_cast<long long>(a.tokens) * csize
+                                       : (static_cast<long long>(a.tokens) + sh.rows - 1) / sh.rows;
+    if (groups > INT_MAX || (csize > 1 && sh.rows != 1))
+        return cudaErrorInvalidConfiguration;
+    const long long push = (static_cast<long long>(a.tokens) * a.units_row + threads - 1) / threads;
+    const long long cap = static_cast<long long>(sms) * per_sm;
+    long long grid = groups > push ? groups : push;
+    if (grid > cap)
+        grid = cap;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid));
+    cfg.blockDim = dim3(threads);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, a, static_cast<uint4*>(lam), sh.tpr, csize, skip_rank);
+}
+
+template <typename T, int R_CT>
+static cudaError_t lamport_vpt(const FusedArgs& a, void* lam, OneShotShape sh, int skip_rank, cudaStream_t s)
+{
+    switch (sh.vpt) {
+    case 1: return run_lamport<T, R_CT, 1>(a, lam, sh, skip_rank, s);
+    case 2: return run_lamport<T, R_CT, 2>(a, lam, sh, skip_rank, s);
+    case 4: return run_lamport<T, R_CT, 4>(a, lam, sh, skip_rank, s);
+    case 8: return run_lamport<T, R_CT, 8>(a, lam, sh, skip_rank, s);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
+template <typename T>
+cudaError_t launch_fused_lamport(const FusedArgs& a, void* lam, OneShotShape sh, int skip_rank, cudaStream_t s)
+{
+    switch (a.R) {
+    case 1: return lamport_vpt<T, 1>(a, lam, sh, skip_rank, s);
+    case 2: return lamport_vpt<T, 2>(a, lam, sh, skip_rank, s);
+    case 4: return lamport_vpt<T, 4>(a, lam, sh, skip_rank, s);
+    case 8: return lamport_vpt<T, 8>(a, lam, sh, skip_rank, s);
+    default: return lamport_vpt<T, 0>(a, lam, sh, skip_rank, s);
+    }
+}
+
+template <typename T>
+cudaError_t launch_lamport_fill(void* buf, size_t bytes, cudaStream_t s)
+{
+    const uint64_t nvec = bytes / 16;
+    const uint32_t tail_halves = static_cast<uint32_t>((bytes % 16) / 2);
+    uint64_t blocks = (nvec + kFlatThreads - 1) / kFlatThreads;
+    if (blocks > 4096)
+        blocks = 4096;
+    if (blocks == 0)
+        blocks = 1;
+    return launch_k(k_lamport_fill<T>, dim3(static_cast<unsigned>(blocks)), dim3(kFlatThreads), 0, s,
+                    static_cast<uint4*>(buf), nvec, tail_halves);
+}
+
 template <typename T>
 cudaError_t take_wait_timeouts(unsigned int* count)
 {
@@ -335,4 +417,7 @@ cudaError_t take_wait_timeouts(unsigned int* count)
     template cudaError_t ar::launch_fused_twoshot<T>(const ar::FusedArgs&, bool, cudaStream_t);     \
     template cudaError_t ar::take_wait_timeouts<T>(unsigned int*);                                  \
     template cudaError_t ar::launch_rmsnorm<T>(const ar::FusedArgs&, bool, ar::OneShotShape, cudaStream_t);      \
-    template cudaError_t ar::launch_rmsnorm_tma<T>(const ar::FusedArgs&, ar::OneShotShape, cudaStream_t);
+    template cudaError_t ar::launch_rmsnorm_tma<T>(const ar::FusedArgs&, ar::OneShotShape, cudaStream_t);     \
+    template cudaError_t ar::launch_fused_lamport<T>(const ar::FusedArgs&, void*, ar::OneShotShape, int,       \
+                                                     cudaStream_t);                                          \
+    template cudaError_t ar::launch_lamport_fill<T>(void*, size_t, cudaStream_t);

@@ -4,6 +4,7 @@
         --R 8 --tokens 1024 --hidden 8192 --dtype bf16 --strategy ONESHOT --calls 3
     python -m tensor_allreduce_residual_gb300.profile_case sum --R 4 --n 33554432 --dtype fp16
     python -m tensor_allreduce_residual_gb300.profile_case rmsnorm --tokens 8192 --hidden 8192 --dtype bf16
+    python -m tensor_allreduce_residual_gb300.profile_case lamport --R 8 --tokens 2048 --hidden 8192
 
 Inputs are the seeded synthetic workloads (drawn on the device), the calls go
 through the C ABI, and nothing is timed or checked: the point is a short,
@@ -23,7 +24,7 @@ if ROOT not in sys.path:
 
 def main(argv=None) -> int:
     p = argparse.ArgumentParser(description="run one library case for a profiler")
-    p.add_argument("op", choices=["fused", "sum", "rmsnorm"])
+    p.add_argument("op", choices=["fused", "sum", "rmsnorm", "lamport"])
     p.add_argument("--R", type=int, default=8)
     p.add_argument("--tokens", type=int, default=1024)
     p.add_argument("--hidden", type=int, default=8192)
@@ -57,10 +58,16 @@ def main(argv=None) -> int:
                                    bias_dist=None if a.no_bias else ("N", 0.0, 0.02),
                                    weight_dist=("N", 1.0, 0.05), eps=1e-6, seed=0, device="cuda")
         out, res = torch.empty_like(f.residual), torch.empty_like(f.residual)
+        if a.op == "lamport":
+            lam = ar.lamport_buffer(a.R, a.hidden, a.tokens, f.residual.dtype)
+            call = lambda: ar.ar_residual_rmsnorm_lamport(f.partials, f.residual, f.weight, f.eps,  # noqa: E731
+                                                          bias=f.bias, out=out, residual_out=res, buffer=lam)
         ws = torch.empty(max(1, ar.ar_workspace_size_rows(a.R, a.hidden, a.tokens, ar.dtype_code(f.residual.dtype))),
                          dtype=torch.uint8, device="cuda")
-        call = lambda: ar.ar_residual_rmsnorm(f.partials, f.residual, f.weight, f.eps, bias=f.bias,  # noqa: E731
-                                              out=out, residual_out=res, intermediate=ws, strategy=a.strategy)
+        if a.op == "fused":
+            call = lambda: ar.ar_residual_rmsnorm(f.partials, f.residual, f.weight, f.eps,  # noqa: E731
+                                                  bias=f.bias, out=out, residual_out=res, intermediate=ws,
+                                                  strategy=a.strategy)
     torch.cuda.synchronize()
     for _ in range(a.warmup + a.calls):
         call()

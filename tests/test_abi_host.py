@@ -39,7 +39,8 @@ def test_header_declares_the_expected_entry_points():
     for want in ["ar_version", "ar_strerror", "ar_workspace_size", "ar_workspace_size_rows", "ar_sum",
                  "ar_residual_rmsnorm", "ar_allreduce", "ar_query_strategy", "ar_query_launch", "ar_device_status",
                  "ar_rmsnorm", "ar_host_staging_size", "ar_residual_rmsnorm_host", "ar_config_workspace_size",
-                 "ar_allreduce_config"]:
+                 "ar_allreduce_config", "ar_lamport_buffer_size", "ar_lamport_init", "ar_lamport_supported",
+                 "ar_residual_rmsnorm_lamport"]:
         assert want in names, names
 
 
@@ -310,6 +311,76 @@ def test_allreduce_config_errors_and_sizes(L):
     assert L.ar_allreduce_config(ctypes.byref(p), 0, ar.AR_ONESHOT, 1, None) == ar.AR_ERR_INVALID_ARG
     p.n = 0
     assert L.ar_allreduce_config(ctypes.byref(p), 0, ar.AR_ONESHOT, 1, None) == ar.AR_OK
+
+
+def _lamport(L, R=2, bias=FAKE + 1 << 20, residual=FAKE + 2 << 20, weight=FAKE + 3 << 20, eps=1e-6,
+             hidden=64, tokens=4, out=FAKE + 4 << 20, residual_out=FAKE + 5 << 20, buf=FAKE + 7 << 20,
+             buf_bytes=1 << 20, dtype=ar.AR_FP32, ptrs=None):
+    return L.ar_residual_rmsnorm_lamport(ptrs if ptrs is not None else _ptrs(R), R, bias, residual, weight,
+                                         ctypes.c_float(eps), hidden, tokens, out, residual_out, buf, buf_bytes,
+                                         dtype, None)
+
+
+def test_lamport_argument_errors(L):
+    assert _lamport(L, R=0) == ar.AR_ERR_INVALID_ARG
+    assert _lamport(L, R=17) == ar.AR_ERR_INVALID_ARG
+    assert _lamport(L, hidden=0) == ar.AR_ERR_INVALID_ARG
+    assert _lamport(L, tokens=-1) == ar.AR_ERR_INVALID_ARG
+    assert _lamport(L, eps=-1.0) == ar.AR_ERR_INVALID_ARG
+    assert _lamport(L, eps=float("nan")) == ar.AR_ERR_INVALID_ARG
+    assert _lamport(L, residual=None) == ar.AR_ERR_INVALID_ARG
+    assert _lamport(L, weight=None) == ar.AR_ERR_INVALID_ARG
+    assert _lamport(L, out=None) == ar.AR_ERR_INVALID_ARG
+    assert _lamport(L, residual_out=FAKE + 4 << 20) == ar.AR_ERR_INVALID_ARG      # out == residual_out
+    bad = _ptrs(2)
+    bad[1] = None
+    assert _lamport(L, ptrs=bad) == ar.AR_ERR_INVALID_ARG
+    assert _lamport(L, dtype=5) == ar.AR_ERR_UNSUPPORTED
+    # only the 16-byte packed path: misaligned pointers, a hidden that is not a multiple of the
+    # lane count, and rows longer than the kernel holds are refused
+    assert _lamport(L, residual=(FAKE + 2 << 20) + 4) == ar.AR_ERR_UNSUPPORTED
+    assert _lamport(L, ptrs=_ptrs(2, FAKE + 8)) == ar.AR_ERR_UNSUPPORTED
+    assert _lamport(L, hidden=66) == ar.AR_ERR_UNSUPPORTED
+    assert _lamport(L, hidden=8192 + 4, tokens=4096, buf_bytes=1 << 30) == ar.AR_ERR_UNSUPPORTED
+    # the buffer: missing, misaligned or short
+    assert _lamport(L, buf=None) == ar.AR_ERR_WORKSPACE
+    assert _lamport(L, buf=(FAKE + 7 << 20) + 8) == ar.AR_ERR_WORKSPACE
+    need = L.ar_lamport_buffer_size(2, 64, 4, ar.AR_FP32)
+    assert need == 2 * 4 * 64 * 4 + 4 * 64                 # the slots, then 64 bytes of exchange area a row
+    assert _lamport(L, buf_bytes=need - 1) == ar.AR_ERR_WORKSPACE
+    assert _lamport(L, buf_bytes=2 * 4 * 64 * 4) == ar.AR_ERR_WORKSPACE
+    # nothing to do
+    assert _lamport(L, tokens=0, buf=None, residual=None, out=None) == ar.AR_OK
+
+
+def test_lamport_buffer_size_support_and_init(L):
+    assert L.ar_lamport_buffer_size(8, 8192, 1, ar.AR_BF16) == (8 * 8192 * 2 + 64 + 255) // 256 * 256
+    assert L.ar_lamport_buffer_size(3, 10, 1, ar.AR_FP16) == 256               # 60 + 64 bytes, rounded up
+    assert L.ar_lamport_buffer_size(8, 8192, 8192, ar.AR_BF16) == 8 * 8192 * 8192 * 2 + 8192 * 64
+    for bad in [(0, 64, 1, ar.AR_FP32), (17, 64, 1, ar.AR_FP32), (2, 0, 1, ar.AR_FP32), (2, 64, -1, ar.AR_FP32),
+                (2, 64, 1, 9)]:
+        assert L.ar_lamport_buffer_size(*bad) == 0
+    w = ctypes.c_int(-1)
+    # up to 8 rows of many vectors: a row split over 4 blocks; else one block a row, 16 warps up to 512 rows
+    assert L.ar_lamport_supported(8, 8192, 1, ar.AR_BF16, ctypes.byref(w)) == ar.AR_OK and w.value == 32
+    assert L.ar_lamport_supported(2, 4096, 32, ar.AR_FP16, ctypes.byref(w)) == ar.AR_OK and w.value == 16
+    assert L.ar_lamport_supported(8, 8192, 256, ar.AR_BF16, ctypes.byref(w)) == ar.AR_OK and w.value == 16
+    assert L.ar_lamport_supported(8, 8192, 4096, ar.AR_BF16, ctypes.byref(w)) == ar.AR_OK and w.value == 8
+    assert L.ar_lamport_supported(2, 16384, 1, ar.AR_BF16, ctypes.byref(w)) == ar.AR_OK and w.value == 8
+    assert L.ar_lamport_supported(2, 16384, 100, ar.AR_BF16, ctypes.byref(w)) == ar.AR_OK and w.value == 8
+    assert L.ar_lamport_supported(2, 64, 4, ar.AR_FP32, ctypes.byref(w)) == ar.AR_OK and w.value == 1
+    assert L.ar_lamport_supported(2, 8192, 1, ar.AR_FP32, None) == ar.AR_OK
+    assert L.ar_lamport_supported(2, 32768, 1000, ar.AR_BF16, None) == ar.AR_ERR_UNSUPPORTED   # row too long
+    assert L.ar_lamport_supported(2, 32768, 1, ar.AR_BF16, ctypes.byref(w)) == ar.AR_OK and w.value == 64
+    assert L.ar_lamport_supported(2, 8 * 32768, 1, ar.AR_BF16, None) == ar.AR_ERR_UNSUPPORTED
+    assert L.ar_lamport_supported(2, 100, 1, ar.AR_BF16, None) == ar.AR_ERR_UNSUPPORTED     # not 8-lane
+    assert L.ar_lamport_supported(0, 64, 1, ar.AR_FP32, None) == ar.AR_ERR_INVALID_ARG
+    assert L.ar_lamport_supported(2, 64, 1, 9, None) == ar.AR_ERR_UNSUPPORTED
+    assert L.ar_lamport_init(None, 16, ar.AR_BF16, None) == ar.AR_ERR_INVALID_ARG
+    assert L.ar_lamport_init(FAKE + 8, 16, ar.AR_BF16, None) == ar.AR_ERR_INVALID_ARG
+    assert L.ar_lamport_init(FAKE, 15, ar.AR_BF16, None) == ar.AR_ERR_INVALID_ARG
+    assert L.ar_lamport_init(FAKE, 16, 9, None) == ar.AR_ERR_UNSUPPORTED
+    assert L.ar_lamport_init(FAKE, 0, ar.AR_BF16, None) == ar.AR_OK
 
 
 def test_launch_plans_are_launchable_for_random_shapes(L):
