@@ -15,16 +15,15 @@
 //
 // On one GPU the R ranks' writes are emulated inside the same launch.  The
 // buffer holds one slot per rank, slot r = [tokens][units_row] 16-byte
-// vectors at r * tokens * units_row.  Every block first pushes its
-// grid-stride share of (row, unit) vectors of all R partials into their
-// slots (the peers' NVLink writes of the multi-GPU protocol), then reduces
-// its rows as the register-resident one-shot kernel does -- tpr threads per
-// row, VPT vectors per thread, fp32 sums in rank order, bias, residual, the
-// row's sum of squares over a fixed tree -- reading each partial from its
-// slot instead of from the partial.  The rows a block reduces were pushed
-// by other blocks, so blocks wait on one another: the launch is cooperative
-// (all of its blocks resident at once, or the launch fails), so every push
-// it waits for is made by a block that is already running.
+// vectors at r * tokens * units_row.  Blocks push vectors of all R partials
+// into their slots (the peers' NVLink writes of the multi-GPU protocol) and
+// reduce rows as the register-resident one-shot kernel does -- tpr threads
+// per row, VPT vectors per thread, fp32 sums in rank order, bias, residual,
+// the row's sum of squares over a fixed tree -- reading each partial from
+// its slot instead of from the partial.  The rows a block reduces were
+// pushed by another block, so blocks wait on one another: the launch is
+// cooperative (all of its blocks resident at once, or the launch fails), so
+// every push it waits for is made by a block that is already running.
 //
 // Memory ordering.  Pushes are st.relaxed.gpu and polls ld.relaxed.gpu, both
 // of 16 bytes: each 2- or 4-byte element is written once, from the marker to
@@ -242,12 +241,51 @@ __device__ __forceinline__ float lamport_exchange(uint32_t* xr, int c, int csize
     return tot;
 }
 
-// The fused kernel.  Packed path only (16-byte vectors).  csize == 1: tpr
-// threads own a row, blockDim.x / tpr rows per block.  csize > 1: a row is
-// split over csize blocks (consecutive groups), block c owning the
-// contiguous slice [c*S, (c+1)*S) of its vectors (S = ceil(units_row /
-// csize)) with all blockDim.x == tpr threads; the slices' sums of squares
-// meet in the exchange area through the same protocol as the data.
+// Pushes vector i of every partial into its rank's slot (skip_rank >= 0:
+// not that rank's).
+template <typename T, int R_CT>
+__device__ __forceinline__ void lamport_push(const FusedArgs& a, uint4* lam, uint64_t slot_units, int R, uint64_t i,
+                                             int skip_rank)
+{
+    if constexpr (R_CT > 0) {
+        uint4 v[R_CT];
+#pragma unroll
+        for (int r = 0; r < R_CT; ++r)
+            v[r] = ld_stream16(static_cast<const uint4*>(a.partials[r]) + i);
+#pragma unroll
+        for (int r = 0; r < R_CT; ++r)
+            if (r != skip_rank)
+                st_relaxed16(lam + r * slot_units + i, lamport_clean<T>(v[r]));
+    } else {
+        for (int r = 0; r < R; ++r) {
+            const uint4 v = ld_stream16(static_cast<const uint4*>(a.partials[r]) + i);
+            if (r != skip_rank)
+                st_relaxed16(lam + r * slot_units + i, lamport_clean<T>(v));
+        }
+    }
+}
+
+// The fused kernel.  Packed path only (16-byte vectors).
+//
+// Work comes in groups.  csize == 1: a group is blockDim.x / tpr rows, tpr
+// threads a row, VPT vectors a thread.  csize > 1: a group is one slice of a
+// row split over csize blocks (consecutive groups), slice c = vectors
+// [c*S, (c+1)*S) with S = ceil(units_row / csize), all blockDim.x == tpr
+// threads on it; the slices' sums of squares meet in the exchange area
+// through the same protocol as the data.
+//
+// Schedule.  The groups are dealt out in steps of gridDim.x: in a step, block
+// b pushes the vectors of group base + b (the very vectors its threads would
+// reduce), then reduces group base + (b + 1) % n, which its neighbour
+// pushes in the same step (n = the step's groups).  Pushes never wait, and a
+// reduce waits only for pushes (and split-row shares) of its own step, so
+// the waits cannot form a cycle; gridDim.x is a multiple of csize, so no
+// split row straddles two steps.  A step's pushed vectors are polled while
+// they are still in L2, and the marker written back over them lands on the
+// same dirty L2 lines: each buffer line reaches DRAM about once instead of
+// being written, read back and written again.  (Pushing one step ahead of
+// the reduce measured slower: with two steps of pushes and the partials'
+// stream in between, the pushed lines left L2 before they were polled.)
 // `skip_rank` >= 0 leaves that rank's pushes out (tests of the bounded waits
 // only; -1 = none).
 template <typename T, int R_CT, int VPT>
@@ -260,31 +298,11 @@ k_fused_lamport(const FusedArgs a, uint4* lam, const int tpr, const int csize, c
     __shared__ float red[2][32];
     __shared__ float tot_s[2];
     const int R = R_CT > 0 ? R_CT : a.R;
+    // Vectors of every rank a thread moves per round.  One: batching more
+    // (16 loads in flight) needed up to 236 registers a thread in the
+    // prefill shape, half the resident warps, and measured slower.
+    constexpr int KB = 1;
     const uint64_t slot_units = static_cast<uint64_t>(a.tokens) * a.units_row;
-
-    // Push: vector i of every partial into its rank's slot.
-    const uint64_t stride = static_cast<uint64_t>(gridDim.x) * blockDim.x;
-    for (uint64_t i = static_cast<uint64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < slot_units; i += stride) {
-        if constexpr (R_CT > 0) {
-            uint4 v[R_CT];
-#pragma unroll
-            for (int r = 0; r < R_CT; ++r)
-                v[r] = ld_stream16(static_cast<const uint4*>(a.partials[r]) + i);
-#pragma unroll
-            for (int r = 0; r < R_CT; ++r)
-                if (r != skip_rank)
-                    st_relaxed16(lam + r * slot_units + i, lamport_clean<T>(v[r]));
-        } else {
-            for (int r = 0; r < R; ++r) {
-                const uint4 v = ld_stream16(static_cast<const uint4*>(a.partials[r]) + i);
-                if (r != skip_rank)
-                    st_relaxed16(lam + r * slot_units + i, lamport_clean<T>(v));
-            }
-        }
-    }
-
-    // Reduce: blocks stride over groups (csize == 1: blockDim.x / tpr rows;
-    // csize > 1: one slice of one row).
     const bool split = csize > 1;
     const int rows = split ? 1 : static_cast<int>(blockDim.x) / tpr;
     const int lane = split ? static_cast<int>(threadIdx.x) : static_cast<int>(threadIdx.x & (tpr - 1));
@@ -292,32 +310,135 @@ k_fused_lamport(const FusedArgs a, uint4* lam, const int tpr, const int csize, c
     const int slice = split ? (a.units_row + csize - 1) / csize : a.units_row;
     const int groups = split ? a.tokens * csize : (a.tokens + rows - 1) / rows;
     uint32_t* xarea = reinterpret_cast<uint32_t*>(lam + static_cast<uint64_t>(R) * slot_units);
+    const int b = static_cast<int>(blockIdx.x);
     bool gave_up = false;
     int parity = 0;
-    for (int g = blockIdx.x; g < groups; g += gridDim.x, parity ^= 1) {
-        const int row = split ? g / csize : g * rows + row_in_block;
-        const int c = split ? g % csize : 0;
+    for (int base = 0; base < groups; base += gridDim.x, parity ^= 1) {
+        const int n = min(static_cast<int>(gridDim.x), groups - base);
+        if (b >= n)
+            break;  // block-uniform: only the last step can be short
+        // The pushed group (this block's) and the reduced one (its neighbour's).
+        const int gp = base + b;
+        const int gr = base + (b + 1) % n;
+        const int p_row = split ? gp / csize : gp * rows + row_in_block;
+        const int p_begin = split ? (gp % csize) * slice : 0;
+        const int p_end = min(p_begin + slice, a.units_row);
+        const bool p_ok = p_row < a.tokens;
+        const uint64_t p_off = static_cast<uint64_t>(p_row) * a.units_row;
+        const int row = split ? gr / csize : gr * rows + row_in_block;
+        const int c = split ? gr % csize : 0;
         const int j_begin = c * slice;
         const int j_end = min(j_begin + slice, a.units_row);
         const bool row_ok = row < a.tokens;
         const uint64_t row_off = static_cast<uint64_t>(row) * a.units_row;
+
+        // The residual of the reduced group does not depend on the buffer:
+        // its loads go out first and complete behind the push.
+        uint4 rv[VPT];
+#pragma unroll
+        for (int k = 0; k < VPT; ++k) {
+            const int j = j_begin + lane + k * tpr;
+            if (row_ok && j < j_end)
+                rv[k] = U::load(a.residual, row_off + j);
+        }
+
+        // Push, KB vectors of every rank per round (up to 16 loads in flight).
+        if constexpr (R_CT > 0) {
+#pragma unroll
+            for (int k0 = 0; k0 < VPT; k0 += KB) {
+                uint4 v[KB][R_CT];
+#pragma unroll
+                for (int kk = 0; kk < KB; ++kk) {
+                    const int j = p_begin + lane + (k0 + kk) * tpr;
+                    if (k0 + kk < VPT && p_ok && j < p_end) {
+#pragma unroll
+                        for (int r = 0; r < R_CT; ++r)
+                            v[kk][r] = ld_stream16(static_cast<const uint4*>(a.partials[r]) + p_off + j);
+                    }
+                }
+#pragma unroll
+                for (int kk = 0; kk < KB; ++kk) {
+                    const int j = p_begin + lane + (k0 + kk) * tpr;
+                    if (k0 + kk < VPT && p_ok && j < p_end) {
+#pragma unroll
+                        for (int r = 0; r < R_CT; ++r)
+                            if (r != skip_rank)
+                                st_relaxed16(lam + r * slot_units + p_off + j, lamport_clean<T>(v[kk][r]));
+                    }
+                }
+            }
+        } else {
+#pragma unroll
+            for (int k = 0; k < VPT; ++k) {
+                const int j = p_begin + lane + k * tpr;
+                if (p_ok && j < p_end)
+                    lamport_push<T, 0>(a, lam, slot_units, R, p_off + j, skip_rank);
+            }
+        }
+
+        // Reduce: take every rank's vector from the buffer (KB vectors of
+        // every rank per round), then bias and residual, in that order.
         float x[VPT][L];
         uint4 wv[VPT];
         float ss = 0.0f;
 #pragma unroll
         for (int k = 0; k < VPT; ++k) {
-            const int j = j_begin + lane + k * tpr;
 #pragma unroll
             for (int l = 0; l < L; ++l)
                 x[k][l] = 0.0f;
+        }
+        if constexpr (R_CT > 0) {
+#pragma unroll
+            for (int k0 = 0; k0 < VPT; k0 += KB) {
+                uint4 v[KB][R_CT];
+#pragma unroll
+                for (int kk = 0; kk < KB; ++kk) {
+                    const int j = j_begin + lane + (k0 + kk) * tpr;
+                    if (k0 + kk < VPT && row_ok && j < j_end) {
+#pragma unroll
+                        for (int r = 0; r < R_CT; ++r)
+                            v[kk][r] = ld_relaxed16(lam + r * slot_units + row_off + j);
+                    }
+                }
+#pragma unroll
+                for (int kk = 0; kk < KB; ++kk) {
+                    const int j = j_begin + lane + (k0 + kk) * tpr;
+                    if (k0 + kk < VPT && row_ok && j < j_end) {
+#pragma unroll
+                        for (int r = 0; r < R_CT; ++r)
+                            v[kk][r] = lamport_poll<T>(lam + r * slot_units + row_off + j, v[kk][r], gave_up);
+#pragma unroll
+                        for (int r = 0; r < R_CT; ++r)
+                            st16(lam + r * slot_units + row_off + j, lamport_empty<T>());
+                        float* xk = x[k0 + kk];
+                        Lanes<T>::unpack(v[kk][0], xk);
+#pragma unroll
+                        for (int r = 1; r < R_CT; ++r) {
+                            float t[L];
+                            Lanes<T>::unpack(v[kk][r], t);
+                            add_lanes<L>(xk, t);
+                        }
+                    }
+                }
+            }
+        } else {
+#pragma unroll
+            for (int k = 0; k < VPT; ++k) {
+                const int j = j_begin + lane + k * tpr;
+                if (row_ok && j < j_end)
+                    lamport_take<T, 0>(lam, slot_units, R, row_off + j, x[k], gave_up);
+            }
+        }
+#pragma unroll
+        for (int k = 0; k < VPT; ++k) {
+            const int j = j_begin + lane + k * tpr;
             if (row_ok && j < j_end) {
-                lamport_take<T, R_CT>(lam, slot_units, R, row_off + j, x[k], gave_up);
                 float t[L];
                 if (a.bias != nullptr) {
                     U::to_float(U::load_cached(a.bias, j), t);
                     add_lanes<L>(x[k], t);
                 }
-                U::to_float(U::load(a.residual, row_off + j), t);
+                U::to_float(rv[k], t);
                 add_lanes<L>(x[k], t);
                 wv[k] = U::load_cached(a.weight, j);
                 U::store(a.residual_out, row_off + j, x[k]);
@@ -327,7 +448,7 @@ k_fused_lamport(const FusedArgs a, uint4* lam, const int tpr, const int csize, c
             }
         }
         // Double-buffered scratch: a warp that runs ahead into the next
-        // group writes the other half.
+        // step writes the other half.
         ss = row_sum(ss, tpr, red[parity]);
         if (split) {
             if (threadIdx.x < 32) {

@@ -315,10 +315,10 @@ cudaError_t launch_fused_twoshot(const FusedArgs& a, bool packed, cudaStream_t s
 }
 
 // Lamport-style fused kernel: one cooperative launch (all blocks resident at
-// once, which its blocks' waits on one another need).  The grid covers the
-// larger of the row groups (rows, or row slices when rows are split) and one
-// pushed vector per thread, capped at the blocks that fit on the device at
-// once; blocks stride over what is left.
+// once, which its blocks' waits on one another need).  One block per row
+// group (rows, or row slices when rows are split), capped at the blocks that
+// fit on the device at once (rounded down to whole split rows); blocks take
+// the groups in steps of the grid.
 template <typename T, int R_CT, int VPT>
 static cudaError_t run_lamport(const FusedArgs& a, void* lam, OneShotShape sh, int skip_rank, cudaStream_t s)
 {
@@ -339,11 +339,11 @@ static cudaError_t run_lamport(const FusedArgs& a, void* lam, OneShotShape sh, i
                                        : (static_cast<long long>(a.tokens) + sh.rows - 1) / sh.rows;
     if (groups > INT_MAX || (csize > 1 && sh.rows != 1))
         return cudaErrorInvalidConfiguration;
-    const long long push = (static_cast<long long>(a.tokens) * a.units_row + threads - 1) / threads;
-    const long long cap = static_cast<long long>(sms) * per_sm;
-    long long grid = groups > push ? groups : push;
-    if (grid > cap)
-        grid = cap;
+    // Whole steps of split rows: the grid is a multiple of csize.
+    const long long cap = static_cast<long long>(sms) * per_sm / csize * csize;
+    if (cap < csize)
+        return cudaErrorInvalidConfiguration;
+    const long long grid = groups < cap ? groups : cap;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(grid));
     cfg.blockDim = dim3(threads);
