@@ -432,6 +432,27 @@ def run_extras(ar, torch, workloads, parts, resid, weight, bias, out, res_out, w
     del tmp
 
     flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    # The prefill curve: R=8 bf16 H=8192 at 512 .. 4096 tokens (90 .. 738 MB
+    # a call) through AUTO.  Cold: L2 flushed before each call, median of 20;
+    # warm: back-to-back calls.
+    peak, _ = measured_peaks()
+    curve = {}
+    for T in (512, 1024, 2048, 4096):
+        f = workloads.tp_prefill(tokens=T, device="cuda")
+        o, r = torch.empty_like(f.residual), torch.empty_like(f.residual)
+        wT = torch.empty(ar.ar_workspace_size_rows(8, 8192, T, ar.AR_BF16), dtype=torch.uint8, device="cuda")
+        fn = lambda f=f, o=o, r=r, wT=wT: ar.ar_residual_rmsnorm(  # noqa: E731
+            f.partials, f.residual, f.weight, f.eps, bias=f.bias, out=o, residual_out=r, intermediate=wT,
+            strategy="AUTO")
+        b = algorithmic_bytes(8, T, 8192, 2, has_bias=True)
+        cold = _time_cold(torch, fn, stream, flush, 20)
+        warm = _time_calls(torch, fn, stream, 50)
+        curve[f"T{T}"] = {"bytes": b, "kernel": ar.ar_query_launch(8, 8192, T, ar.AR_BF16, "AUTO")["kernel_name"],
+                          "us_cold": round(cold * 1e3, 2), "GBps_cold": round(b / cold / 1e6, 1),
+                          "frac_cold": round(b / cold / 1e6 / peak, 4),
+                          "us_warm": round(warm * 1e3, 2), "GBps_warm": round(b / warm / 1e6, 1)}
+        del f, o, r, wT
+    ex["prefill_curve_R8_bf16_H8192_AUTO"] = curve
     # PR1 reference case: R=2 fp32, 4 x 64, fusion NONE and RESIDUAL_RMS_NORM.
     p1 = workloads.pr1(seed=0)
     p1d = [t.cuda() for t in p1.partials]

@@ -28,7 +28,9 @@
  *     one call has the same element type (ar_dtype); eps is a float.
  *   - Alignment: 16-byte aligned pointers (and, for the fused call, hidden a
  *     multiple of 16/sizeof(element)) take the 16-byte packed path; anything
- *     else takes a slower element-wise path.  Misalignment is not an error.
+ *     else takes a slower element-wise path.  Misalignment is not an error,
+ *     except for ar_residual_rmsnorm_lamport, which has the packed path only
+ *     and returns AR_ERR_UNSUPPORTED.
  *   - Aliasing: out may be one of partials[r] and residual_out may be
  *     residual (each element is read before it is written).  out and
  *     residual_out must differ.  Any other overlap is undefined.
@@ -36,7 +38,9 @@
  *   - Determinism: the sum of every element is accumulated in fp32 in the
  *     fixed order partials[0], ..., partials[R-1], bias, residual, and every
  *     row reduction uses a fixed tree, so results are bit-identical from run
- *     to run.  residual_out is also bit-identical across strategies.
+ *     to run.  residual_out is also bit-identical across strategies, and
+ *     equal in value through the Lamport-style call (which may flip the sign
+ *     of an exact zero).
  */
 #ifndef TENSOR_ALLREDUCE_RESIDUAL_AR_H
 #define TENSOR_ALLREDUCE_RESIDUAL_AR_H
