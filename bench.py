@@ -330,17 +330,32 @@ def _time_calls(torch, fn, stream, n, warm=3):
 
 
 def _time_cold(torch, fn, stream, flush, n):
-    """Median per-call time with L2 flushed (a 256 MB write) before every call."""
+    """Mean per-call time with L2 flushed before every call.
+
+    One event pair per call: on this GPU an event interval resolves only
+    2.048 us, so each sample is quantized.  The mean of the samples averages
+    the quantization out (the median would sit on a multiple of 2.048 us).
+
+    `flush` is two buffers larger than L2: the first is written, then the
+    second is read, so that the timed call finds L2 holding clean lines of
+    the second buffer only.  (With the write alone, the timed call also paid
+    for writing back up to an L2's worth of the flush's dirty lines.)  A
+    fixed 50,000-cycle device sleep then keeps the GPU busy while the host
+    enqueues the timed call, so the events bracket device time only, not the
+    host's launch latency.
+    """
     ts = []
     for _ in range(n):
-        flush.zero_()
+        flush[0].zero_()
+        flush[1].amax()
+        torch.cuda._sleep(50000)
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record(stream)
         fn()
         b.record(stream)
         torch.cuda.synchronize()
         ts.append(a.elapsed_time(b))
-    return statistics.median(ts)
+    return statistics.mean(ts)
 
 
 def _time_graph(torch, fn, n=20, reps=5):
@@ -431,9 +446,10 @@ def run_extras(ar, torch, workloads, parts, resid, weight, bias, out, res_out, w
     ex["prefill_rmsnorm_alone"] = {"us_per_call": round(ms * 1e3, 2), "bytes": nb, "GBps": round(nb / ms / 1e6, 1)}
     del tmp
 
-    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    flush = (torch.empty(256 << 20, dtype=torch.uint8, device="cuda"),
+             torch.zeros(256 << 20, dtype=torch.uint8, device="cuda"))
     # The prefill curve: R=8 bf16 H=8192 at 512 .. 4096 tokens (90 .. 738 MB
-    # a call) through AUTO.  Cold: L2 flushed before each call, median of 20;
+    # a call) through AUTO.  Cold: L2 flushed before each call, mean of 20;
     # warm: back-to-back calls.
     peak, _ = measured_peaks()
     curve = {}
