@@ -1,6 +1,7 @@
 """The library from plain C: tests/c_abi_example.c is compiled with gcc
 against include/ar.h, linked with libar.so and the CUDA runtime, and run; its
-fused output, residual_out and plain sum are checked against the oracle.
+fused output, residual_out, plain sum and Lamport-style outputs are checked
+against the oracle.
 Nothing on that path goes through Python or torch."""
 import os
 import shutil
@@ -42,9 +43,11 @@ def test_c_program_through_the_abi(tmp_path):
     res = subprocess.run([str(exe), str(inp), str(outp)], capture_output=True, text=True, timeout=120)
     assert res.returncode == 0 and "c_abi_example: ok" in res.stdout, res.stdout + res.stderr
 
-    got = torch.from_numpy(np.fromfile(outp, dtype=np.float32)).reshape(3, T, H)
+    got = torch.from_numpy(np.fromfile(outp, dtype=np.float32)).reshape(5, T, H)
     ref_out, ref_res, inv = oracle.residual_rmsnorm(f.partials, f.bias, f.residual, f.weight, EPS, "fp32")
     terms = [p.reshape(T, H) for p in f.partials] + [f.bias.expand(T, H).contiguous(), f.residual]
     tol.check_sum(got[1], ref_res, terms, "fp32", "residual_out")
     tol.check_fused_out(got[0], ref_out, terms, f.weight, inv, "fp32", H, "out")
     tol.check_sum(got[2], oracle.sum(f.partials, "fp32"), f.partials, "fp32", "sum")
+    tol.check_sum(got[4], ref_res, terms, "fp32", "Lamport residual_out")
+    tol.check_fused_out(got[3], ref_out, terms, f.weight, inv, "fp32", H, "Lamport out")
