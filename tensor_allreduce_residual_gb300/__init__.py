@@ -180,6 +180,42 @@ def _check(func: str, status: int):
         raise ARError(func, status)
 
 
+def _fused_pointers(partials, residual, weight, bias, out, residual_out, host=False):
+    """Pointers of a fused call's tensors, in one pass that checks each: the size and dtype the call
+    reads or writes (the library trusts its pointers, so a short or wrongly typed tensor would be
+    read or written past its end), contiguity, and the device (residual's GPU; the host for host
+    calls).  Names are built only for an error message.
+
+    Returns (tokens, hidden, partial pointer array, bias, residual, weight, out, residual_out)."""
+    if residual.dim() != 2:
+        raise ValueError("residual must be [tokens, hidden]")
+    if len(partials) == 0:
+        raise ValueError("at least one partial is needed")
+    tokens, hidden = residual.shape
+    n = tokens * hidden
+    dt = residual.dtype
+    dev = residual.get_device()
+    if host != (dev < 0):
+        raise ValueError("residual must be a host (CPU) tensor" if host else "residual must be a CUDA tensor")
+
+    def fail(name, numel):
+        where = "the host" if host else f"cuda:{dev}"
+        raise ValueError(f"{name} must be a contiguous tensor of {numel} {dt} elements on {where}")
+
+    addrs = []
+    for p in partials:
+        if p.numel() != n or p.dtype != dt or p.get_device() != dev or not p.is_contiguous():
+            fail(f"partials[{len(addrs)}]", n)
+        addrs.append(p.data_ptr())
+    got = [None] * 5
+    for i, (t, numel) in enumerate(((bias, hidden), (residual, n), (weight, hidden), (out, n), (residual_out, n))):
+        if t is not None:
+            if t.numel() != numel or t.dtype != dt or t.get_device() != dev or not t.is_contiguous():
+                fail(("bias", "residual", "weight", "out", "residual_out")[i], numel)
+            got[i] = t.data_ptr()
+    return (tokens, hidden, _ptr_array(addrs), *got)
+
+
 # ------------------------------------------------------------------ the ABI
 
 def ar_version() -> int:
@@ -236,8 +272,8 @@ def ar_sum(partials: Sequence[torch.Tensor], out: Optional[torch.Tensor] = None,
             raise ValueError(f"partials[{k}] does not match partials[0] in shape, dtype or device")
     if out is None:
         out = torch.empty_like(p0)
-    elif out.numel() != p0.numel() or out.dtype != p0.dtype:
-        raise ValueError("out must match the partials in size and dtype")
+    elif out.numel() != p0.numel() or out.dtype != p0.dtype or out.device != device:
+        raise ValueError("out must match the partials in size, dtype and device")
     ptrs = _ptr_array([_dev_ptr(p, f"partials[{k}]") for k, p in enumerate(partials)])
     status = lib().ar_sum(ptrs, len(partials), _dev_ptr(out, "out"), p0.numel(), dtype_code(p0.dtype),
                           _strategy(strategy), _stream_handle(stream))
@@ -255,18 +291,13 @@ def ar_residual_rmsnorm(partials: Sequence[torch.Tensor], residual: torch.Tensor
     ar_workspace_size_rows(...) bytes); when it is None and the strategy may
     take the two-shot path, one is allocated with torch.
     """
-    if residual.dim() != 2:
-        raise ValueError("residual must be [tokens, hidden]")
-    tokens, hidden = residual.shape
-    n, dt = residual.numel(), residual.dtype
-    for k, p in enumerate(partials):
-        if p.numel() != n or p.dtype != dt:
-            raise ValueError(f"partials[{k}] must match residual in size and dtype")
     if out is None:
         out = torch.empty_like(residual)
     if residual_out is None:
         residual_out = torch.empty_like(residual)
-    code = dtype_code(dt)
+    tokens, hidden, ptrs, p_bias, p_res, p_w, p_out, p_rout = _fused_pointers(
+        partials, residual, weight, bias, out, residual_out)
+    code = dtype_code(residual.dtype)
     st = _strategy(strategy)
     if intermediate is None and st in (AR_TWOSHOT, AR_AUTO):
         need = ar_workspace_size_rows(len(partials), hidden, tokens, code)
@@ -274,11 +305,8 @@ def ar_residual_rmsnorm(partials: Sequence[torch.Tensor], residual: torch.Tensor
             intermediate = torch.empty(need, dtype=torch.uint8, device=residual.device)
     ws_ptr = _dev_ptr(intermediate, "intermediate")
     ws_bytes = 0 if intermediate is None else intermediate.numel() * intermediate.element_size()
-    ptrs = _ptr_array([_dev_ptr(p, f"partials[{k}]") for k, p in enumerate(partials)])
-    status = lib().ar_residual_rmsnorm(
-        ptrs, len(partials), _dev_ptr(bias, "bias"), _dev_ptr(residual, "residual"),
-        _dev_ptr(weight, "weight"), eps, hidden, tokens, _dev_ptr(out, "out"),
-        _dev_ptr(residual_out, "residual_out"), ws_ptr, ws_bytes, code, st, _stream_handle(stream))
+    status = lib().ar_residual_rmsnorm(ptrs, len(partials), p_bias, p_res, p_w, eps, hidden, tokens, p_out, p_rout,
+                                       ws_ptr, ws_bytes, code, st, _stream_handle(stream))
     _check("ar_residual_rmsnorm", status)
     return out, residual_out
 
@@ -292,19 +320,13 @@ def ar_residual_rmsnorm_noalloc(partials: Sequence[torch.Tensor], residual: torc
     and ``residual_out`` are required (this wrapper creates no tensor either).
     Accepts shapes with ar_workspace_size_rows(...) <= AR_NOALLOC_SCRATCH_BYTES.
     """
-    if residual.dim() != 2:
-        raise ValueError("residual must be [tokens, hidden]")
     if out is None or residual_out is None:
         raise ValueError("out and residual_out must be given: this call allocates nothing")
-    tokens, hidden = residual.shape
-    for k, p in enumerate(partials):
-        if p.numel() != residual.numel() or p.dtype != residual.dtype:
-            raise ValueError(f"partials[{k}] must match residual in size and dtype")
-    ptrs = _ptr_array([_dev_ptr(p, f"partials[{k}]") for k, p in enumerate(partials)])
-    status = lib().ar_residual_rmsnorm_noalloc(
-        ptrs, len(partials), _dev_ptr(bias, "bias"), _dev_ptr(residual, "residual"),
-        _dev_ptr(weight, "weight"), ctypes.c_float(eps), hidden, tokens, _dev_ptr(out, "out"),
-        _dev_ptr(residual_out, "residual_out"), dtype_code(residual.dtype), _stream_handle(stream))
+    tokens, hidden, ptrs, p_bias, p_res, p_w, p_out, p_rout = _fused_pointers(
+        partials, residual, weight, bias, out, residual_out)
+    status = lib().ar_residual_rmsnorm_noalloc(ptrs, len(partials), p_bias, p_res, p_w, ctypes.c_float(eps), hidden,
+                                               tokens, p_out, p_rout, dtype_code(residual.dtype),
+                                               _stream_handle(stream))
     _check("ar_residual_rmsnorm_noalloc", status)
     return out, residual_out
 
@@ -315,12 +337,12 @@ def ar_rmsnorm(x: torch.Tensor, weight: torch.Tensor, eps: float, out: Optional[
     if x.dim() != 2:
         raise ValueError("x must be [tokens, hidden]")
     tokens, hidden = x.shape
-    if weight.numel() != hidden or weight.dtype != x.dtype:
-        raise ValueError("weight must be [hidden] of x's dtype")
+    if weight.numel() != hidden or weight.dtype != x.dtype or weight.device != x.device:
+        raise ValueError("weight must be [hidden] of x's dtype, on x's device")
     if out is None:
         out = torch.empty_like(x)
-    elif out.numel() != x.numel() or out.dtype != x.dtype:
-        raise ValueError("out must match x in size and dtype")
+    elif out.numel() != x.numel() or out.dtype != x.dtype or out.device != x.device:
+        raise ValueError("out must match x in size, dtype and device")
     _check("ar_rmsnorm", lib().ar_rmsnorm(_dev_ptr(x, "x"), _dev_ptr(weight, "weight"), ctypes.c_float(eps), hidden,
                                           tokens, _dev_ptr(out, "out"), dtype_code(x.dtype), _stream_handle(stream)))
     return out
@@ -349,13 +371,12 @@ def ar_residual_rmsnorm_host(partials: Sequence[torch.Tensor], residual: torch.T
 
     Asynchronous: synchronise `stream` before reading out / residual_out.
     """
-    if residual.dim() != 2:
-        raise ValueError("residual must be [tokens, hidden]")
-    tokens, hidden = residual.shape
-    ptrs = _ptr_array([_host_ptr(p, f"partials[{k}]") for k, p in enumerate(partials)])
+    if out is None or residual_out is None:
+        raise ValueError("out and residual_out must be given (host tensors)")
+    tokens, hidden, ptrs, p_bias, p_res, p_w, p_out, p_rout = _fused_pointers(
+        partials, residual, weight, bias, out, residual_out, host=True)
     status = lib().ar_residual_rmsnorm_host(
-        ptrs, len(partials), _host_ptr(bias, "bias"), _host_ptr(residual, "residual"), _host_ptr(weight, "weight"),
-        ctypes.c_float(eps), hidden, tokens, _host_ptr(out, "out"), _host_ptr(residual_out, "residual_out"),
+        ptrs, len(partials), p_bias, p_res, p_w, ctypes.c_float(eps), hidden, tokens, p_out, p_rout,
         _dev_ptr(staging, "staging"), staging.numel() * staging.element_size(), chunk_tokens,
         dtype_code(residual.dtype), _strategy(strategy), _stream_handle(stream))
     _check("ar_residual_rmsnorm_host", status)
@@ -442,23 +463,17 @@ def ar_residual_rmsnorm_lamport(partials: Sequence[torch.Tensor], residual: torc
     completed call leaves it filled again, so one buffer serves a sequence of
     calls on one stream.  When it is None a new one is made for this call.
     """
-    if residual.dim() != 2:
-        raise ValueError("residual must be [tokens, hidden]")
-    tokens, hidden = residual.shape
-    for k, p in enumerate(partials):
-        if p.numel() != residual.numel() or p.dtype != residual.dtype:
-            raise ValueError(f"partials[{k}] must match residual in size and dtype")
     if out is None:
         out = torch.empty_like(residual)
     if residual_out is None:
         residual_out = torch.empty_like(residual)
+    tokens, hidden, ptrs, p_bias, p_res, p_w, p_out, p_rout = _fused_pointers(
+        partials, residual, weight, bias, out, residual_out)
     if buffer is None:
         buffer = lamport_buffer(len(partials), hidden, tokens, residual.dtype, residual.device)
-    ptrs = _ptr_array([_dev_ptr(p, f"partials[{k}]") for k, p in enumerate(partials)])
     status = lib().ar_residual_rmsnorm_lamport(
-        ptrs, len(partials), _dev_ptr(bias, "bias"), _dev_ptr(residual, "residual"),
-        _dev_ptr(weight, "weight"), ctypes.c_float(eps), hidden, tokens, _dev_ptr(out, "out"),
-        _dev_ptr(residual_out, "residual_out"), _dev_ptr(buffer, "buffer"),
-        buffer.numel() * buffer.element_size(), dtype_code(residual.dtype), _stream_handle(stream))
+        ptrs, len(partials), p_bias, p_res, p_w, ctypes.c_float(eps), hidden, tokens, p_out, p_rout,
+        _dev_ptr(buffer, "buffer"), buffer.numel() * buffer.element_size(), dtype_code(residual.dtype),
+        _stream_handle(stream))
     _check("ar_residual_rmsnorm_lamport", status)
     return out, residual_out

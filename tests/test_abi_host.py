@@ -419,3 +419,48 @@ def test_launch_plans_are_launchable_for_random_shapes(L):
             assert p["threads_per_row"] * p["units_per_thread"] >= units
             assert p["threads_per_row"] & (p["threads_per_row"] - 1) == 0
     assert {1, 4, 5, 6} <= seen, seen      # the draw reached the main kernels
+
+
+def test_binding_rejects_mismatched_tensors_before_any_call():
+    """The Python binding checks every tensor's size, dtype, device and layout against the call's shape
+    before it reaches the library (which trusts its pointers).  Host tensors exercise the checks without
+    a GPU: the host-buffer call takes them, the device calls refuse them."""
+    import torch
+    T, H = 4, 64
+    bf = torch.bfloat16
+    parts = [torch.zeros(T, H, dtype=bf) for _ in range(2)]
+    res, w, b = torch.zeros(T, H, dtype=bf), torch.ones(H, dtype=bf), torch.zeros(H, dtype=bf)
+    out, rout = torch.zeros(T, H, dtype=bf), torch.zeros(T, H, dtype=bf)
+    staging = torch.zeros(16, dtype=torch.uint8)
+
+    def host(**kw):
+        args = dict(partials=parts, residual=res, weight=w, eps=1e-6, staging=staging, out=out, residual_out=rout,
+                    bias=b)
+        args.update(kw)
+        return ar.ar_residual_rmsnorm_host(**args)
+
+    bad_cases = [
+        dict(weight=torch.ones(H - 8, dtype=bf)),                      # short weight
+        dict(weight=torch.ones(H, dtype=torch.float16)),               # wrong dtype
+        dict(bias=torch.zeros(2 * H, dtype=bf)),                       # long bias
+        dict(out=torch.zeros(T - 1, H, dtype=bf)),                     # short output
+        dict(residual_out=torch.zeros(T, H, dtype=torch.float32)),     # wrong dtype
+        dict(partials=[parts[0], torch.zeros(T, H + 8, dtype=bf)]),    # partial of another shape
+        dict(partials=[parts[0], torch.zeros(H, T, dtype=bf).t()]),    # not contiguous
+        dict(partials=[]),                                             # no partials
+        dict(residual=torch.zeros(T * H, dtype=bf)),                   # not [tokens, hidden]
+        dict(out=None),                                                # host outputs are required
+    ]
+    for kw in bad_cases:
+        with pytest.raises(ValueError):
+            host(**kw)
+    # device calls refuse host tensors outright
+    for call in (lambda: ar.ar_residual_rmsnorm(parts, res, w, 1e-6, bias=b, out=out, residual_out=rout),
+                 lambda: ar.ar_residual_rmsnorm_lamport(parts, res, w, 1e-6, bias=b, out=out, residual_out=rout),
+                 lambda: ar.ar_residual_rmsnorm_noalloc(parts, res, w, 1e-6, bias=b, out=out, residual_out=rout),
+                 lambda: ar.ar_rmsnorm(res, w, 1e-6, out=out),
+                 lambda: ar.ar_sum(parts, out=out)):
+        with pytest.raises(ValueError):
+            call()
+    with pytest.raises(ValueError):
+        ar.ar_rmsnorm(res, torch.ones(H + 8, dtype=bf), 1e-6)
