@@ -344,6 +344,8 @@ def _time_cold(torch, fn, stream, flush, n):
     enqueues the timed call, so the events bracket device time only, not the
     host's launch latency.
     """
+    fn()  # a first call loads the kernel: not a sample
+    torch.cuda.synchronize()
     ts = []
     for _ in range(n):
         flush[0].zero_()
