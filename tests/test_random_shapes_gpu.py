@@ -4,7 +4,8 @@ The fixed workloads cover the measured configurations; this draws rank
 counts 1..16, all three element types, rows from 1 to 16384 elements (packed
 and element-wise), 1 to 3000 rows (enough to reach the bulk-copy-fed kernel
 by rule) and optional bias, and checks out and residual_out of each call
-against the oracle with the usual tolerance.  Sizes are bounded so the oracle
+(and of the Lamport-style call, where it takes the shape) against the oracle
+with the usual tolerance.  Sizes are bounded so the oracle
 stays within seconds."""
 import random
 
@@ -76,3 +77,11 @@ def test_random_shape_matches_oracle(R, dt, H, T, has_bias, strategy, seed):
     s = ar.ar_sum(parts, strategy="TWOSHOT" if strategy == "TWOSHOT" else "ONESHOT")
     torch.cuda.synchronize()
     tol.check_sum(s.cpu(), oracle.sum(f.partials, dt), f.partials, dt, "sum")
+    # and the Lamport-style call, wherever it takes the shape
+    if ar.ar_lamport_supported(R, H, T, workloads.DTYPES[dt]) is not None:
+        lo, lr = ar.ar_residual_rmsnorm_lamport(parts, f.residual.cuda(), f.weight.cuda(), f.eps,
+                                                bias=None if f.bias is None else f.bias.cuda())
+        torch.cuda.synchronize()
+        tol.check_sum(lr.cpu(), ref_res, terms, dt, "Lamport residual_out")
+        tol.check_fused_out(lo.cpu(), ref_out, terms, f.weight, inv, dt, H, "Lamport out")
+        assert ar.ar_device_status() == ar.AR_OK
