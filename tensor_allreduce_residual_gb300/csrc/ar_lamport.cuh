@@ -298,10 +298,6 @@ k_fused_lamport(const FusedArgs a, uint4* lam, const int tpr, const int csize, c
     __shared__ float red[2][32];
     __shared__ float tot_s[2];
     const int R = R_CT > 0 ? R_CT : a.R;
-    // Vectors of every rank a thread moves per round.  One: batching more
-    // (16 loads in flight) needed up to 236 registers a thread in the
-    // prefill shape, half the resident warps, and measured slower.
-    constexpr int KB = 1;
     const uint64_t slot_units = static_cast<uint64_t>(a.tokens) * a.units_row;
     const bool split = csize > 1;
     const int rows = split ? 1 : static_cast<int>(blockDim.x) / tpr;
@@ -342,92 +338,27 @@ k_fused_lamport(const FusedArgs a, uint4* lam, const int tpr, const int csize, c
                 rv[k] = U::load(a.residual, row_off + j);
         }
 
-        // Push, KB vectors of every rank per round (up to 16 loads in flight).
-        if constexpr (R_CT > 0) {
+        // Push: vector by vector, all R ranks' loads in flight at once.
 #pragma unroll
-            for (int k0 = 0; k0 < VPT; k0 += KB) {
-                uint4 v[KB][R_CT];
-#pragma unroll
-                for (int kk = 0; kk < KB; ++kk) {
-                    const int j = p_begin + lane + (k0 + kk) * tpr;
-                    if (k0 + kk < VPT && p_ok && j < p_end) {
-#pragma unroll
-                        for (int r = 0; r < R_CT; ++r)
-                            v[kk][r] = ld_stream16(static_cast<const uint4*>(a.partials[r]) + p_off + j);
-                    }
-                }
-#pragma unroll
-                for (int kk = 0; kk < KB; ++kk) {
-                    const int j = p_begin + lane + (k0 + kk) * tpr;
-                    if (k0 + kk < VPT && p_ok && j < p_end) {
-#pragma unroll
-                        for (int r = 0; r < R_CT; ++r)
-                            if (r != skip_rank)
-                                st_relaxed16(lam + r * slot_units + p_off + j, lamport_clean<T>(v[kk][r]));
-                    }
-                }
-            }
-        } else {
-#pragma unroll
-            for (int k = 0; k < VPT; ++k) {
-                const int j = p_begin + lane + k * tpr;
-                if (p_ok && j < p_end)
-                    lamport_push<T, 0>(a, lam, slot_units, R, p_off + j, skip_rank);
-            }
+        for (int k = 0; k < VPT; ++k) {
+            const int j = p_begin + lane + k * tpr;
+            if (p_ok && j < p_end)
+                lamport_push<T, R_CT>(a, lam, slot_units, R, p_off + j, skip_rank);
         }
 
-        // Reduce: take every rank's vector from the buffer (KB vectors of
-        // every rank per round), then bias and residual, in that order.
+        // Reduce: take every rank's vector from the buffer, then bias and
+        // residual, in that order.
         float x[VPT][L];
         uint4 wv[VPT];
         float ss = 0.0f;
 #pragma unroll
         for (int k = 0; k < VPT; ++k) {
+            const int j = j_begin + lane + k * tpr;
 #pragma unroll
             for (int l = 0; l < L; ++l)
                 x[k][l] = 0.0f;
-        }
-        if constexpr (R_CT > 0) {
-#pragma unroll
-            for (int k0 = 0; k0 < VPT; k0 += KB) {
-                uint4 v[KB][R_CT];
-#pragma unroll
-                for (int kk = 0; kk < KB; ++kk) {
-                    const int j = j_begin + lane + (k0 + kk) * tpr;
-                    if (k0 + kk < VPT && row_ok && j < j_end) {
-#pragma unroll
-                        for (int r = 0; r < R_CT; ++r)
-                            v[kk][r] = ld_relaxed16(lam + r * slot_units + row_off + j);
-                    }
-                }
-#pragma unroll
-                for (int kk = 0; kk < KB; ++kk) {
-                    const int j = j_begin + lane + (k0 + kk) * tpr;
-                    if (k0 + kk < VPT && row_ok && j < j_end) {
-#pragma unroll
-                        for (int r = 0; r < R_CT; ++r)
-                            v[kk][r] = lamport_poll<T>(lam + r * slot_units + row_off + j, v[kk][r], gave_up);
-#pragma unroll
-                        for (int r = 0; r < R_CT; ++r)
-                            st16(lam + r * slot_units + row_off + j, lamport_empty<T>());
-                        float* xk = x[k0 + kk];
-                        Lanes<T>::unpack(v[kk][0], xk);
-#pragma unroll
-                        for (int r = 1; r < R_CT; ++r) {
-                            float t[L];
-                            Lanes<T>::unpack(v[kk][r], t);
-                            add_lanes<L>(xk, t);
-                        }
-                    }
-                }
-            }
-        } else {
-#pragma unroll
-            for (int k = 0; k < VPT; ++k) {
-                const int j = j_begin + lane + k * tpr;
-                if (row_ok && j < j_end)
-                    lamport_take<T, 0>(lam, slot_units, R, row_off + j, x[k], gave_up);
-            }
+            if (row_ok && j < j_end)
+                lamport_take<T, R_CT>(lam, slot_units, R, row_off + j, x[k], gave_up);
         }
 #pragma unroll
         for (int k = 0; k < VPT; ++k) {
