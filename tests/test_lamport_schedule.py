@@ -1,0 +1,106 @@
+"""A CPU model of the Lamport-style kernel's schedule, checked before trusting it on a GPU.
+
+The kernel deals its groups (rows, or row slices when a row is split over
+C blocks) out in steps of the grid: in a step, block b pushes group
+base + b and then reduces group base + (b + 1) % n, n being the step's
+groups; a split row's blocks exchange their shares of the sum of squares and
+wait for all C of them.  Blocks wait on one another, so the schedule must
+(1) push and reduce every group exactly once, (2) keep every split row's
+slices in one step, and (3) have no cycle among its waits, whatever the
+grid.  This model states those rules independently of the CUDA code and
+checks them for many token counts, splits and grids, including a grid
+rounded down to whole split rows as the launcher does.
+"""
+import random
+from collections import defaultdict, deque
+
+import pytest
+
+
+def schedule(groups, G):
+    """[(step, block, pushed group, reduced group)] for every block that works in a step."""
+    out = []
+    step = 0
+    for base in range(0, groups, G):
+        n = min(G, groups - base)
+        for b in range(n):
+            out.append((step, b, base + b, base + (b + 1) % n))
+        step += 1
+    return out
+
+
+def check(tokens, csize, rows, G):
+    groups = tokens * csize if csize > 1 else -(-tokens // rows)
+    if csize > 1:
+        assert G % csize == 0
+    sched = schedule(groups, G)
+    pushed = [g for _, _, g, _ in sched]
+    reduced = [g for _, _, _, g in sched]
+    assert sorted(pushed) == list(range(groups))
+    assert sorted(reduced) == list(range(groups))
+    step_of = {g: s for s, _, g, _ in sched}
+    if csize > 1:   # all slices of a row are reduced in one step
+        for row in range(tokens):
+            assert len({step_of[row * csize + c] for c in range(csize)}) == 1
+
+    # Wait graph.  Nodes: ("push", s, b), ("share", s, b) = its reduce has read its data and written
+    # its share, ("done", s, b) = its reduce is complete.  Edges point from what must happen first.
+    edges = defaultdict(set)
+    nodes = set()
+    pusher = {g: (s, b) for s, b, g, _ in sched}
+    by_block = defaultdict(list)
+    for s, b, gp, gr in sched:
+        by_block[b].append((s, gr))
+        nodes |= {("push", s, b), ("share", s, b), ("done", s, b)}
+        edges[("push", s, b)].add(("share", s, b))              # program order
+        edges[("share", s, b)].add(("done", s, b))
+        ps, pb = pusher[gr]
+        edges[("push", ps, pb)].add(("share", s, b))            # the reduce polls the pushed group
+    for b, steps in by_block.items():                           # program order across steps
+        steps.sort()
+        for (s0, _), (s1, _) in zip(steps, steps[1:]):
+            edges[("done", s0, b)].add(("push", s1, b))
+    if csize > 1:                                               # a split row's exchange waits for every share
+        reducer = {g: (s, b) for s, b, _, g in sched}
+        for row in range(tokens):
+            members = [reducer[row * csize + c] for c in range(csize)]
+            for (s0, b0) in members:
+                for (s1, b1) in members:
+                    edges[("share", s0, b0)].add(("done", s1, b1))
+    # Kahn's algorithm: every node must come out, or the waits contain a cycle.
+    indeg = {v: 0 for v in nodes}
+    for u in edges:
+        for v in edges[u]:
+            indeg[v] += 1
+    ready = deque(v for v in nodes if indeg[v] == 0)
+    seen = 0
+    while ready:
+        u = ready.popleft()
+        seen += 1
+        for v in edges.get(u, ()):
+            indeg[v] -= 1
+            if indeg[v] == 0:
+                ready.append(v)
+    assert seen == len(nodes), f"waits form a cycle: tokens={tokens} csize={csize} rows={rows} G={G}"
+
+
+@pytest.mark.parametrize("csize", [1, 2, 4, 8])
+def test_schedule_covers_every_group_once_without_cycles(csize):
+    rng = random.Random(csize)
+    for _ in range(150):
+        tokens = rng.choice([1, 2, 3, 7, 8, 16, 33, 100, 257, rng.randint(1, 700)])
+        rows = 1 if csize > 1 else rng.choice([1, 2, 4, 8])
+        groups = tokens * csize if csize > 1 else -(-tokens // rows)
+        resident = rng.choice([1, 2, 5, 152, 304, 456, rng.randint(1, 1000)])
+        cap = resident // csize * csize               # the launcher's rounding to whole split rows
+        if cap < csize:
+            continue
+        check(tokens, csize, rows, min(groups, cap))
+
+
+def test_grid_not_a_multiple_of_the_split_would_straddle_steps():
+    """Why the launcher rounds the grid down to whole split rows: with 6 blocks and rows split over 4,
+    the second row's slices fall into two steps."""
+    groups, G, csize = 8, 6, 4
+    step_of = {gr: s for s, _, _, gr in schedule(groups, G)}
+    assert len({step_of[4 + c] for c in range(csize)}) == 2
