@@ -29,17 +29,16 @@ def schedule(groups, G):
     return out
 
 
-def check(tokens, csize, rows, G):
+def check(tokens, csize, rows, G, launcher_grid=True):
     groups = tokens * csize if csize > 1 else -(-tokens // rows)
-    if csize > 1:
-        assert G % csize == 0
     sched = schedule(groups, G)
     pushed = [g for _, _, g, _ in sched]
     reduced = [g for _, _, _, g in sched]
     assert sorted(pushed) == list(range(groups))
     assert sorted(reduced) == list(range(groups))
     step_of = {g: s for s, _, g, _ in sched}
-    if csize > 1:   # all slices of a row are reduced in one step
+    if csize > 1 and launcher_grid:   # the launcher's grid: all slices of a row are reduced in one step
+        assert G % csize == 0
         for row in range(tokens):
             assert len({step_of[row * csize + c] for c in range(csize)}) == 1
 
@@ -104,3 +103,12 @@ def test_grid_not_a_multiple_of_the_split_would_straddle_steps():
     groups, G, csize = 8, 6, 4
     step_of = {gr: s for s, _, _, gr in schedule(groups, G)}
     assert len({step_of[4 + c] for c in range(csize)}) == 2
+
+
+def test_the_model_finds_the_cycle_of_a_straddling_row():
+    """The model has teeth: one row split over 4 blocks on a grid of 3 (which the launcher never
+    makes).  Block 0 reduces slice 1 in step 0 and slice 3 in step 1, so its exchange in step 0 waits
+    for a share it would only write after leaving step 0: a cycle."""
+    with pytest.raises(AssertionError, match="cycle"):
+        check(1, 4, 1, 3, launcher_grid=False)
+    check(1, 4, 1, 4)   # the launcher's grid for this call
