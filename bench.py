@@ -544,6 +544,14 @@ def run_extras(ar, torch, workloads, parts, resid, weight, bias, out, res_out, w
             row[s] = {"us": round(ms * 1e3, 2), "GBps": round(b / ms / 1e6, 1)}
         red[f"2^{k}"] = row
     ex["reduce_only_R4_fp16_sweep"] = red
+    # R=1 (the tpSize=1 passthrough): a copy into another buffer, and the
+    # in-place call, which launches nothing.
+    src = big.partials[0]
+    b1 = workloads.sum_algorithmic_bytes(1, src.numel(), "fp16")
+    ms = _time_calls(torch, lambda: ar.ar_sum([src], out=o_big), stream, 20)
+    ms_in = _time_calls(torch, lambda: ar.ar_sum([src], out=src), stream, 200)
+    ex["r1_passthrough_fp16_2^27"] = {"copy_us": round(ms * 1e3, 2), "copy_GBps": round(b1 / ms / 1e6, 1),
+                                      "in_place_us": round(ms_in * 1e3, 2)}
     del big, o_big
     torch.cuda.empty_cache()
     return ex
