@@ -46,7 +46,8 @@ static const AutoEntry kAutoTable[] = {
     {2, 3, 512, 2147483647, 1, 1, 3, 1, 1, 4},  // R3_fp16_H4096 T=8192: one-shot 62.422 us
     {2, 4, 1024, 1, 1, 1, 4, 0, 8, 0},  // R4_fp16_H8192 T=1: one-shot 3.123 us
     {2, 4, 1024, 64, 1, 2, 0, 1, 1, 0},  // R4_fp16_H8192 T=64: one-shot 3.414 us
-    {2, 4, 1024, 1024, 1, 1, 3, 1, 1, 8},  // R4_fp16_H8192 T=1024: one-shot 18.016 us
+    {2, 4, 1024, 512, 1, 2, 0, 1, 1, 0},  // R4_fp16_H8192 T=65..512: the register shape that ran for T=1024's pick
+    {2, 4, 1024, 1024, 1, 4, 0, 1, 1, 0},  // R4_fp16_H8192 T=1024: one-shot 18.016 us (register shape)
     {2, 4, 1024, 4096, 1, 4, 3, 1, 1, 4},  // R4_fp16_H8192 T=4096: one-shot 70.666 us
     {2, 4, 1024, 2147483647, 1, 4, 3, 1, 1, 4},  // R4_fp16_H8192 T=8192: one-shot 137.034 us
     {2, 8, 512, 1, 1, 1, 4, 0, 8, 0},  // R8_bf16_H4096 T=1: one-shot 2.966 us

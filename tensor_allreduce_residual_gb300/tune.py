@@ -40,6 +40,31 @@ SHAPES = ([f"{v}:{m}:{e}" for v in (1, 2, 4, 8) for m in (0, 1) for e in (0, 1)]
           + [f"{v}:4:1:{c}" for v in (1, 2, 4) for c in (2, 4, 8)])
 
 
+# OneShotMode of a shape -> the ar_kernel codes a launch plan may report for it (the persistent
+# mode runs as shared-memory rows where its kernel cannot take the row).
+KERNEL_OF_MODE = {0: (1,), 1: (2,), 2: (2, 3), 3: (4,), 4: (6,)}
+
+
+def shape_taken(plan: dict, shape: str) -> bool:
+    """Whether a launch plan (ar_query_launch) is the one-shot shape "vpt:mode[:early[:bps[:stages]]]"
+    that was asked for.  A shape that does not fit the row falls back to the rule's shape, and a
+    sweep must not record that time under the name of the shape it asked for."""
+    f = [int(x) for x in shape.split(":")]
+    vpt, mode = f[0], f[1]
+    early = int(len(f) > 2 and f[2] != 0)
+    bps = f[3] if len(f) > 3 and f[3] > 0 else 1
+    stages = f[4] if len(f) > 4 else 0
+    if plan["strategy"] != 1 or plan["kernel"] not in KERNEL_OF_MODE.get(mode, ()):
+        return False
+    if plan["units_per_thread"] != vpt or plan["early_residual"] != early:
+        return False
+    if mode == 4 and plan["cluster"] != bps:
+        return False
+    if mode == 3 and (plan["blocks_per_sm"] != bps or (stages > 0 and plan["stages"] > stages)):
+        return False
+    return True
+
+
 def _graph_time(torch, fn, n=10, reps=5):
     for _ in range(3):
         fn()
@@ -77,6 +102,14 @@ def _measure(strategy: str, shape: str, out, cases=None, token_filter=None):
         for T in tokens:
             if token_filter and T not in token_filter:
                 continue
+            if strategy == "ONESHOT" and shape != "-":
+                code = {"fp32": ar.AR_FP32, "fp16": ar.AR_FP16, "bf16": ar.AR_BF16}[dtype]
+                try:
+                    plan = ar.ar_query_launch(R, H, T, code, "ONESHOT")
+                except ar.ARError:
+                    continue   # no one-shot kernel holds this row
+                if not shape_taken(plan, shape):
+                    continue   # the shape does not fit this row: the rule's shape would run instead
             f = workloads.fused_inputs(R, T, H, dtype, partial_dist=("N", 0.0, 1.0 / R),
                                        residual_dist=("N", 0.0, 4.0),
                                        bias_dist=("N", 0.0, 0.02) if has_bias else None,
