@@ -462,10 +462,12 @@ def test_allreduce_config_flags_match_allreduce(config, strategy):
 
 
 @pytest.mark.parametrize("R,dtype,H,T", [(16, "bf16", 8192, 5), (16, "bf16", 8192, 64), (16, "bf16", 8192, 300),
-                                         (3, "fp16", 4096, 64), (3, "fp16", 4096, 2100)])
+                                         (3, "fp16", 4096, 64), (3, "fp16", 4096, 2100),
+                                         (4, "fp16", 8192, 100), (4, "fp16", 8192, 700)])
 def test_measured_rank_counts_through_auto(R, dtype, H, T):
     """R=16 and R=3 rows through the kernels the measured table picks for them (row-split cluster
-    kernel at few tokens, bulk-copy-fed persistent kernel with R outside the compiled rank counts)."""
+    kernel at few tokens, bulk-copy-fed persistent kernel with R outside the compiled rank counts),
+    and R=4 fp16 rows of 8192 through the table's register shapes on both sides of 512 tokens."""
     f = workloads.fused_inputs(R, T, H, dtype, partial_dist=("N", 0.0, 1.0 / R), residual_dist=("N", 0.0, 4.0),
                                bias_dist=("N", 0.0, 0.02), weight_dist=("N", 1.0, 0.05), eps=1e-6, seed=R * T)
     kernel = ar.ar_query_launch(R, H, T, ar.dtype_code(TD[dtype]))["kernel_name"]
