@@ -409,8 +409,16 @@ def test_launch_plans_are_launchable_for_random_shapes(L):
         assert p["smem_bytes"] <= 227 * 1024, p
         units = hidden // lanes_of[dt] if hidden % lanes_of[dt] == 0 else hidden
         if p["kernel"] == 4:       # bulk-copy ring: consumers + producer warp, whole chunks, two stages at least
-            assert p["threads_per_block"] == p["threads_per_row"] + 32 and p["threads_per_row"] % 32 == 0
-            assert p["threads_per_row"] * p["units_per_thread"] >= units and p["stages"] >= 2
+            nc, cpr, stages = p["threads_per_row"], p["units_per_thread"], p["stages"]
+            assert p["threads_per_block"] == nc + 32 and nc % 32 == 0
+            assert nc * cpr >= units and stages >= 2
+            assert -(-units // nc) <= cpr              # the row's chunks fit the compiled chunk count
+            # ring layout: per stage the R partials' and the residual's chunk tiles (16-byte vectors),
+            # then a full and an empty mbarrier per stage, then the [2][32] fp32 row-reduction scratch
+            tiles = stages * (R + 1) * nc * 16
+            assert tiles % 16 == 0 and p["smem_bytes"] == tiles + stages * 16 + 2 * 32 * 4
+            last = units - (-(-units // nc) - 1) * nc  # vectors in a row's last (ragged) chunk
+            assert 0 < last <= nc
             assert p["smem_bytes"] * p["blocks_per_sm"] <= 228 * 1024 - 1024 * p["blocks_per_sm"]
         elif p["kernel"] == 6:     # row split over a cluster
             assert p["cluster"] in (2, 4, 8) and p["threads_per_row"] == p["threads_per_block"] * p["cluster"]
