@@ -47,18 +47,24 @@ __device__ __forceinline__ void pdl_enter()
 // ---------------------------------------------------------------------------
 
 // Streaming 16-byte load: read-only path, not kept in L1 (each byte is read
-// exactly once by exactly one thread).
+// exactly once by exactly one thread).  The statement is volatile and clobbers
+// memory so that the compiler keeps it after pdl_enter()'s griddepcontrol.wait
+// and after any earlier store: several kernels read what the previous kernel
+// in the stream wrote (two-shot phase 2 reads phase 1's residual_out, the norm
+// reads a sum), and a load hoisted above the wait would see stale data.
 __device__ __forceinline__ uint4 ld_stream16(const void* p)
 {
     uint4 r;
 #if AR_L2_PREFETCH_256B
-    asm("ld.global.nc.L1::no_allocate.L2::256B.v4.u32 {%0, %1, %2, %3}, [%4];"
-        : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
-        : "l"(p));
+    asm volatile("ld.global.nc.L1::no_allocate.L2::256B.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+                 : "l"(p)
+                 : "memory");
 #else
-    asm("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
-        : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
-        : "l"(p));
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+                 : "l"(p)
+                 : "memory");
 #endif
     return r;
 }
