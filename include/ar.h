@@ -389,7 +389,11 @@ int ar_device_status(void);
  * Set-up: the first call on a device, with that device current, looks up
  *   the array's device address (cudaGetSymbolAddress) and keeps it for
  *   later calls; make that first call before any stream capture begins.
- *   A failed look-up returns AR_ERR_CUDA.
+ *   The address is kept together with the id of the CUDA context it
+ *   belongs to: after cudaDeviceReset (which destroys the array with its
+ *   context), or from another context the caller has made current, the
+ *   next call looks the address up again, and that call too belongs before
+ *   any stream capture.  A failed look-up returns AR_ERR_CUDA.
  * Sharing: all calls on a device use the same array and it keeps what the
  *   last call wrote.  Each call writes every entry it reads before reading
  *   it, so nothing is cleared between calls.  Calls whose work overlaps on
