@@ -19,6 +19,10 @@ import torch
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libar.so")
+# The same library with its test hooks compiled in (launch-shape override,
+# bounded-wait fault injection, programmatic-launch switch, read from the
+# environment); only tests and shape sweeps load it, by use_test_library().
+TEST_LIB_PATH = os.path.join(_PKG, "libar_test.so")
 
 # ar_dtype
 AR_FP32, AR_FP16, AR_BF16 = 0, 1, 2
@@ -77,16 +81,27 @@ KERNEL_NAMES = {1: "k_fused_oneshot", 2: "k_fused_oneshot", 3: "k_fused_oneshot_
                 4: "k_fused_oneshot_tma", 5: "k_twoshot_phase1+k_twoshot_phase2", 6: "k_fused_oneshot_cluster"}
 
 _lib: Optional[ctypes.CDLL] = None
+_lib_path = LIB_PATH
+
+
+def use_test_library() -> None:
+    """Load libar_test.so instead of libar.so in this process (tests and shape sweeps only: its launch
+    shapes and fault injection follow AR_ONESHOT_SHAPE, AR_TEST_STALL_STAGE, AR_TEST_LAMPORT_SKIP_RANK
+    and AR_PDL).  Must come before the first call into the library."""
+    global _lib_path
+    if _lib is not None and _lib_path != TEST_LIB_PATH:
+        raise RuntimeError("libar.so is already loaded in this process")
+    _lib_path = TEST_LIB_PATH
 
 
 def lib() -> ctypes.CDLL:
-    """The loaded libar.so with its C signatures declared.  Raises if it is not built."""
+    """The loaded libar.so (or libar_test.so) with its C signatures declared.  Raises if it is not built."""
     global _lib
     if _lib is not None:
         return _lib
-    if not os.path.exists(LIB_PATH):
-        raise RuntimeError(f"{LIB_PATH} is missing: build it first (tensor_allreduce_residual_gb300._build.build())")
-    L = ctypes.CDLL(LIB_PATH)
+    if not os.path.exists(_lib_path):
+        raise RuntimeError(f"{_lib_path} is missing: build it first (tensor_allreduce_residual_gb300._build.build())")
+    L = ctypes.CDLL(_lib_path)
     vp, sz, i = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int
     pvp = ctypes.POINTER(ctypes.c_void_p)
     L.ar_version.argtypes, L.ar_version.restype = [], i

@@ -2,6 +2,14 @@
 
 The translation units compile in parallel, then link into one shared
 library next to this file.  Nothing is installed anywhere else.
+
+A second library, libar_test.so, is the same code with the test hooks
+compiled in (AR_TEST_HOOKS: the launch-shape override, the fault injection
+of the bounded-wait tests and the programmatic-launch switch, each read from
+the environment).  Only ar_api.cu differs, so only it is compiled twice.
+The tests of forced launch shapes and of bounded waits, and the shape sweeps
+that build the AUTO table, load it; everything else loads libar.so, which
+reads no environment variable.
 """
 from __future__ import annotations
 
@@ -16,6 +24,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libar.so")
+TEST_LIB = os.path.join(PKG, "libar_test.so")
 
 SOURCES = ["ar_api.cu", "ar_kern_f32.cu", "ar_kern_f16.cu", "ar_kern_bf16.cu", "ar_noalloc.cu", "ar_host.cu"]
 HEADERS = ["ar_internal.h", "ar_kernels.cuh", "ar_tma.cuh", "ar_lamport.cuh", "ar_launch.cuh", "ar_auto_table.h"]
@@ -33,24 +42,25 @@ def nvcc() -> str:
 
 
 def _stale() -> bool:
-    if not os.path.exists(LIB):
+    if not (os.path.exists(LIB) and os.path.exists(TEST_LIB)):
         return True
-    t = os.path.getmtime(LIB)
+    t = min(os.path.getmtime(LIB), os.path.getmtime(TEST_LIB))
     deps = [os.path.join(CSRC, f) for f in SOURCES + HEADERS] + [os.path.join(INCLUDE, "ar.h"), __file__]
     return any(os.path.getmtime(d) > t for d in deps)
 
 
 def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) -> str:
-    """Compile and link libar.so if any source is newer than it; returns its path."""
+    """Compile and link libar.so and libar_test.so if any source is newer; returns libar.so's path."""
     if not force and not _stale():
         return LIB
     os.makedirs(BUILD, exist_ok=True)
     cc = nvcc()
     procs = []
     objs = []
-    for src in SOURCES:
-        obj = os.path.join(BUILD, src.replace(".cu", ".o"))
-        cmd = [cc, *ARCH, *FLAGS, "-c", os.path.join(CSRC, src), "-o", obj]
+    units = [(src, os.path.join(BUILD, src.replace(".cu", ".o")), []) for src in SOURCES]
+    units.append(("ar_api.cu", os.path.join(BUILD, "ar_api_test.o"), ["-DAR_TEST_HOOKS"]))
+    for src, obj, defs in units:
+        cmd = [cc, *ARCH, *FLAGS, *defs, "-c", os.path.join(CSRC, src), "-o", obj]
         if ptxas_info:
             cmd.insert(1, "-Xptxas=-v")
         if verbose:
@@ -66,9 +76,12 @@ def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) 
             failed.append(src)
     if failed:
         raise RuntimeError(f"nvcc failed on {failed}")
-    tmp = f"{LIB}.{os.getpid()}.tmp"
-    subprocess.run([cc, *ARCH, "-shared", "-o", tmp, *objs], check=True)
-    os.replace(tmp, LIB)
+    product = objs[:len(SOURCES)]
+    test = [o if not o.endswith(os.sep + "ar_api.o") else objs[-1] for o in product]
+    for lib, lib_objs in ((LIB, product), (TEST_LIB, test)):
+        tmp = f"{lib}.{os.getpid()}.tmp"
+        subprocess.run([cc, *ARCH, "-shared", "-o", tmp, *lib_objs], check=True)
+        os.replace(tmp, lib)
     return LIB
 
 

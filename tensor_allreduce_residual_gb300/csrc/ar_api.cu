@@ -211,12 +211,40 @@ const ar::AutoEntry* table_lookup(int esize, int R, int units_row, int tokens)
     return nullptr;
 }
 
-// Measurement override of the one-shot shape: AR_ONESHOT_SHAPE="vpt:mode",
-// "vpt:mode:early", "vpt:mode:early:blocks_per_sm" or
-// "vpt:mode:early:blocks_per_sm:max_stages" (e.g. "4:1", "2:0:1", "4:3:0:2",
-// "4:3:1:1:3"; for mode 4 the fourth field is the cluster size, "1:4:1:8")
-// replaces the table and the rule for every packed call.  Read once per
-// process; used to sweep shapes when building the AUTO table.
+// AR_AUTO's partition for the reduce-only sum of n elements: the measured
+// table (keyed on n in 16-byte vectors), else the rule -- R rank slices when
+// the one-slice grid would have fewer blocks than the rank-slice grid (small
+// n: more blocks in flight, less latency), one slice otherwise.  `units` is
+// what the kernel walks: vectors on the packed path, elements otherwise.
+// Both partitions give bit-identical values.
+int sum_auto_strategy(int esize, int R, size_t n, bool packed)
+{
+    if (R == 1)
+        return AR_ONESHOT;
+    const uint64_t vectors = n / static_cast<size_t>(16 / esize);
+    for (const ar::SumAutoEntry& e : ar::kSumAutoTable) {
+        if (e.esize == 0)
+            break;
+        if (e.esize == esize && e.R == R && vectors <= static_cast<uint64_t>(e.units_max))
+            return e.strategy;
+    }
+    const uint64_t units = packed ? vectors : n;
+    const uint64_t per_block = static_cast<uint64_t>(ar::kFlatThreads) * ar::sum_unroll(R, packed);
+    const uint64_t one = (units + per_block - 1) / per_block;
+    const uint64_t slice = (units + R - 1) / R;
+    const uint64_t two = static_cast<uint64_t>(R) * ((slice + per_block - 1) / per_block);
+    return one < two ? AR_TWOSHOT : AR_ONESHOT;
+}
+
+// Measurement override of the one-shot shape.  Only the test build of the
+// library (compiled with AR_TEST_HOOKS, libar_test.so) reads it, from
+// AR_ONESHOT_SHAPE="vpt:mode", "vpt:mode:early", "vpt:mode:early:blocks_per_sm"
+// or "vpt:mode:early:blocks_per_sm:max_stages" (e.g. "4:1", "2:0:1",
+// "4:3:0:2", "4:3:1:1:3"; for mode 4 the fourth field is the cluster size,
+// "1:4:1:8"), once per process; it then replaces the table and the rule for
+// every packed call.  The sweeps that build the AUTO table and the tests of
+// every launch shape use it.  The product library never reads the
+// environment: its override is always empty.
 struct ShapeOverride {
     int vpt = 0;
     int mode = 0;
@@ -225,6 +253,7 @@ struct ShapeOverride {
     int max_stages = 0;
 };
 
+#ifdef AR_TEST_HOOKS
 const ShapeOverride& shape_override()
 {
     static const ShapeOverride ov = [] {
@@ -245,11 +274,11 @@ const ShapeOverride& shape_override()
     return ov;
 }
 
-// Test-only fault injection for the bulk-copy-fed kernel's bounded waits:
-// AR_TEST_STALL_STAGE=k makes its producer leave stage k of every block
-// unarmed, so the waits on it run out (about a second) and the kernel takes
-// its abort path; ar_device_status then reports AR_ERR_TIMEOUT.  Read once
-// per process; unset means no stall.
+// Fault injection for the bulk-copy-fed kernel's bounded waits (test build
+// only): AR_TEST_STALL_STAGE=k makes its producer leave stage k of every
+// block unarmed, so the waits on it run out (about a second) and the kernel
+// takes its abort path; ar_device_status then reports AR_ERR_TIMEOUT.  Read
+// once per process; unset means no stall.
 int test_stall_stage()
 {
     static const int v = [] {
@@ -259,6 +288,29 @@ int test_stall_stage()
     }();
     return v;
 }
+
+// Fault injection for the Lamport call's bounded waits (test build only):
+// AR_TEST_LAMPORT_SKIP_RANK=r leaves rank r's pushes out, so the polls of
+// its slot run out (about a second); ar_device_status then reports
+// AR_ERR_TIMEOUT.  Read once per process; unset means -1 (none).
+int test_lamport_skip_rank()
+{
+    static const int v = [] {
+        const char* e = std::getenv("AR_TEST_LAMPORT_SKIP_RANK");
+        const int r = e != nullptr ? std::atoi(e) : -1;
+        return r >= 0 && r < AR_MAX_RANKS ? r : -1;
+    }();
+    return v;
+}
+#else
+const ShapeOverride& shape_override()
+{
+    static const ShapeOverride none;
+    return none;
+}
+int test_stall_stage() { return 0; }
+int test_lamport_skip_rank() { return -1; }
+#endif
 
 struct FusedPlan {
     int strategy;      // AR_ONESHOT or AR_TWOSHOT
@@ -422,21 +474,26 @@ size_t lamport_buffer_bytes(int R, int hidden, int tokens, int esize)
            static_cast<size_t>(tokens) * ar::kLamportRowWords * sizeof(uint32_t);
 }
 
-// Test-only fault injection for the Lamport call's bounded waits:
-// AR_TEST_LAMPORT_SKIP_RANK=r leaves rank r's pushes out, so the polls of
-// its slot run out (about a second); ar_device_status then reports
-// AR_ERR_TIMEOUT.  Read once per process; unset means -1 (none).
-int test_lamport_skip_rank()
+}  // namespace
+
+namespace ar {
+
+// Programmatic dependent launch is always on in the product library; the
+// test build switches it off with AR_PDL=0 (read once), to measure its effect.
+bool pdl_enabled()
 {
-    static const int v = [] {
-        const char* e = std::getenv("AR_TEST_LAMPORT_SKIP_RANK");
-        const int r = e != nullptr ? std::atoi(e) : -1;
-        return r >= 0 && r < AR_MAX_RANKS ? r : -1;
+#ifdef AR_TEST_HOOKS
+    static const bool on = [] {
+        const char* e = std::getenv("AR_PDL");
+        return !(e != nullptr && e[0] == '0');
     }();
-    return v;
+    return on;
+#else
+    return true;
+#endif
 }
 
-}  // namespace
+}  // namespace ar
 
 extern "C" {
 
@@ -504,8 +561,11 @@ int ar_sum(const void* const* partials, int R, void* out, size_t n, int dtype, i
     a.nunits = packed ? n / lanes : n;
     a.tail = packed ? static_cast<uint32_t>(n % lanes) : 0u;
 
-    // Both strategies give bit-identical values; AUTO takes the one-shot
-    // partition (the two-shot slices only change which block reads what).
+    // Both strategies give bit-identical values (the two-shot slices only
+    // change which block reads what); AUTO takes the partition measured
+    // faster for this size.
+    if (strategy == AR_AUTO)
+        strategy = sum_auto_strategy(esize, R, n, packed);
     int nslices = 1;
     if (strategy == AR_TWOSHOT && R > 1) {
         a.slice = (a.nunits + R - 1) / R;
@@ -812,7 +872,8 @@ int ar_query_strategy(int R, size_t n, int hidden, int dtype, int fusion_op, int
     if (esize == 0)
         return AR_ERR_UNSUPPORTED;
     if (fusion_op == AR_FUSION_NONE) {
-        *chosen = AR_ONESHOT;
+        // The partition of the packed path (16-byte aligned pointers).
+        *chosen = sum_auto_strategy(esize, R, n, true);
         if (warps_per_token)
             *warps_per_token = 0;
         return AR_OK;

@@ -72,4 +72,22 @@ static const AutoEntry kAutoTable[] = {
     {0, 0, 0, 0, 0, 0, 0, 0, 0, 0},  // sentinel
 };
 
+// Measured choices for AR_AUTO on the reduce-only path (ar_sum, fusion
+// NONE): which work partition was faster -- one slice over all blocks
+// (strategy 1, the one-shot partition) or R rank slices (strategy 2, the
+// two-shot reduce-scatter) -- per (element size, R), for n up to `units_max`
+// 16-byte vectors (n / lanes).  Both partitions give bit-identical values,
+// so the choice is speed only.  The first matching entry wins; an (element
+// size, R) with no entry falls back to the rule in ar_api.cu.
+struct SumAutoEntry {
+    int esize;            // bytes per element
+    int R;                // partials
+    long long units_max;  // entry applies to nunits <= units_max
+    int strategy;         // 1 = one slice, 2 = R rank slices
+};
+
+static const SumAutoEntry kSumAutoTable[] = {
+    {0, 0, 0, 0},  // sentinel
+};
+
 }  // namespace ar

@@ -18,6 +18,13 @@ constexpr int kMaxRanks = 16;
 // Threads per block of the flat kernels (reduce-only, two-shot phases).
 constexpr int kFlatThreads = 256;
 
+// Units each thread of the reduce-only kernel sums per launch (R * UNROLL
+// loads in flight per thread): fewer for more partials, to bound registers.
+__host__ __device__ constexpr int sum_unroll(int R, bool packed)
+{
+    return !packed ? 4 : (R <= 2 ? 8 : (R <= 4 ? 4 : 2));
+}
+
 // Two-shot fused path: vectors per thread per chunk.  A chunk is
 // kFlatThreads * kChunkVPT packed vectors of one row.
 constexpr int kChunkVPT = 2;
@@ -86,8 +93,8 @@ struct FusedArgs {
     int chunk_units;       // two-shot units per chunk
     float eps;
     int early_residual;    // one-shot: write residual_out before the row barrier
-    int stall_stage;       // tests only: the bulk-copy producer leaves stage (stall_stage - 1)
-                           // of every block unarmed; 0 (the zero-initialised value) = none
+    int stall_stage;       // test build only: the bulk-copy producer leaves stage (stall_stage - 1)
+                           // of every block unarmed; always 0 (none) in the product library
 };
 
 // Where the one-shot fused kernel keeps a row's fp32 sums between the sum and
@@ -147,6 +154,10 @@ __host__ __device__ constexpr size_t tma_smem_bytes(int inputs, int nc, int stag
 {
     return static_cast<size_t>(stages) * inputs * nc * 16 + static_cast<size_t>(stages) * 16 + 2 * 32 * 4;
 }
+
+// Whether launches carry the programmatic-stream-serialization attribute
+// (defined in ar_api.cu: always in the product library).
+bool pdl_enabled();
 
 // Launchers, explicitly instantiated for float, __half and __nv_bfloat16 in
 // the per-dtype translation units.  Each returns the cudaError_t of the launch.

@@ -10,7 +10,6 @@
 #pragma once
 
 #include <climits>
-#include <cstdlib>
 #include <utility>
 
 #include "ar_kernels.cuh"
@@ -18,17 +17,6 @@
 #include "ar_tma.cuh"
 
 namespace ar {
-
-// Programmatic dependent launch is on unless AR_PDL=0 (read once; kept for
-// measuring its effect).
-inline bool pdl_enabled()
-{
-    static const bool on = [] {
-        const char* e = std::getenv("AR_PDL");
-        return !(e != nullptr && e[0] == '0');
-    }();
-    return on;
-}
 
 // Launches `kernel` on `s` with the programmatic-stream-serialization
 // attribute (see pdl_enter in ar_kernels.cuh); returns the launch status.
@@ -66,17 +54,17 @@ template <typename T>
 cudaError_t launch_sum(const SumArgs& a, bool packed, int nslices, cudaStream_t s)
 {
     if (!packed)
-        return run_sum<T, false, 0, 4>(a, nslices, s);
+        return run_sum<T, false, 0, sum_unroll(0, false)>(a, nslices, s);
     switch (a.R) {
-    case 1: return run_sum<T, true, 1, 8>(a, nslices, s);
-    case 2: return run_sum<T, true, 2, 8>(a, nslices, s);
-    case 3: return run_sum<T, true, 3, 4>(a, nslices, s);
-    case 4: return run_sum<T, true, 4, 4>(a, nslices, s);
-    case 5: return run_sum<T, true, 5, 2>(a, nslices, s);
-    case 6: return run_sum<T, true, 6, 2>(a, nslices, s);
-    case 7: return run_sum<T, true, 7, 2>(a, nslices, s);
-    case 8: return run_sum<T, true, 8, 2>(a, nslices, s);
-    default: return run_sum<T, true, 0, 2>(a, nslices, s);
+    case 1: return run_sum<T, true, 1, sum_unroll(1, true)>(a, nslices, s);
+    case 2: return run_sum<T, true, 2, sum_unroll(2, true)>(a, nslices, s);
+    case 3: return run_sum<T, true, 3, sum_unroll(3, true)>(a, nslices, s);
+    case 4: return run_sum<T, true, 4, sum_unroll(4, true)>(a, nslices, s);
+    case 5: return run_sum<T, true, 5, sum_unroll(5, true)>(a, nslices, s);
+    case 6: return run_sum<T, true, 6, sum_unroll(6, true)>(a, nslices, s);
+    case 7: return run_sum<T, true, 7, sum_unroll(7, true)>(a, nslices, s);
+    case 8: return run_sum<T, true, 8, sum_unroll(8, true)>(a, nslices, s);
+    default: return run_sum<T, true, 0, sum_unroll(16, true)>(a, nslices, s);
     }
 }
 

@@ -10,6 +10,8 @@ Inputs are the seeded synthetic workloads (drawn on the device), the calls go
 through the C ABI, and nothing is timed or checked: the point is a short,
 deterministic launch sequence that `ncu -k <kernel> -s <skip> -c <count>`
 can select from.  `--warmup` calls run first, then `--calls` more.
+`--test-library` loads libar_test.so, whose launch shape follows
+AR_ONESHOT_SHAPE (to profile a shape AUTO does not pick).
 """
 from __future__ import annotations
 
@@ -34,6 +36,7 @@ def main(argv=None) -> int:
     p.add_argument("--no-bias", action="store_true")
     p.add_argument("--warmup", type=int, default=2)
     p.add_argument("--calls", type=int, default=3)
+    p.add_argument("--test-library", action="store_true", help="load libar_test.so (AR_ONESHOT_SHAPE applies)")
     a = p.parse_args(argv)
 
     import torch
@@ -41,6 +44,8 @@ def main(argv=None) -> int:
     import tensor_allreduce_residual_gb300 as ar
     import workloads
 
+    if a.test_library:
+        ar.use_test_library()
     torch.cuda.set_device(0)
     ar.lib()
     if a.op == "sum":

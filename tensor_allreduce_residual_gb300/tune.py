@@ -2,15 +2,24 @@
 
     python -m tensor_allreduce_residual_gb300.tune sweep results.jsonl [--cases A,B] [--shapes S1,S2] [--tokens T1,T2]
     python -m tensor_allreduce_residual_gb300.tune table results.jsonl
+    python -m tensor_allreduce_residual_gb300.tune sumsweep sums.jsonl
+    python -m tensor_allreduce_residual_gb300.tune sumtable sums.jsonl
 
 `sweep` times every one-shot shape (units per thread x where the row is kept
 x when residual_out is written) and the two-shot path on the row shapes of
 the measured workloads, each shape in its own process (the shape override
-AR_ONESHOT_SHAPE is read once per process).  Calls are captured in a CUDA
+AR_ONESHOT_SHAPE is read once per process, by the test build libar_test.so,
+which the children load).  Calls are captured in a CUDA
 graph and replayed, so the numbers are device time without Python launch
 overhead.  `table` keeps the fastest choice per (element size, R, row
 length, tokens) and rewrites csrc/ar_auto_table.h.  This is the measured
 counterpart of heuristic_min_warp_number / selectImplementation.
+
+`sumsweep` times the reduce-only call's two work partitions (one slice, R
+rank slices) for n = 2^9 .. 2^27 elements at several rank counts and element
+sizes, each point as the median of 11 replays of a graph of up to 100 calls
+(enough to resolve 0.1 us at the smallest sizes); `sumtable` keeps the faster
+partition per point and writes the reduce-only table of the same header.
 """
 from __future__ import annotations
 
@@ -95,6 +104,7 @@ def _measure(strategy: str, shape: str, out, cases=None, token_filter=None):
 
     import tensor_allreduce_residual_gb300 as ar
     import workloads
+    ar.use_test_library()
     torch.cuda.set_device(0)
     for name, R, dtype, H, has_bias, tokens in CASES:
         if cases and name not in cases:
@@ -190,6 +200,88 @@ def table(path: str):
     print(f"wrote {len(lines)} entries to {TABLE}")
 
 
+SUM_RANKS = (2, 3, 4, 8, 16)
+SUM_DTYPES = ("fp16", "fp32")
+SUM_LOG2N = range(9, 28)
+
+
+def _graph_time_precise(torch, fn, est_us):
+    """Median over 11 replays of a graph of up to 100 calls (about 20 ms of work per replay at most)."""
+    n = max(3, min(100, int(20000 / max(est_us, 1.0))))
+    return _graph_time(torch, fn, n=n, reps=11)
+
+
+def sum_sweep(path: str):
+    sys.path.insert(0, ROOT)
+    import torch
+
+    import tensor_allreduce_residual_gb300 as ar
+    import workloads
+    torch.cuda.set_device(0)
+    with open(path, "w") as out:
+        for dtype in SUM_DTYPES:
+            es = workloads.ELEM_SIZE[dtype]
+            for R in SUM_RANKS:
+                nmax = 1 << max(SUM_LOG2N)
+                big = workloads.sum_inputs(R, nmax, dtype, ("U", -1.0, 1.0), seed=R, device="cuda")
+                o_big = torch.empty_like(big.partials[0])
+                for k in SUM_LOG2N:
+                    n = 1 << k
+                    parts = [p[:n] for p in big.partials]
+                    o = o_big[:n]
+                    est = (R + 1) * n * es / 6.5e3 + 2.0   # us at about 6.5 TB/s, plus the launch
+                    for strategy in ("ONESHOT", "TWOSHOT"):
+                        us = _graph_time_precise(
+                            torch, lambda s=strategy: ar.ar_sum(parts, out=o, strategy=s), est) * 1e3
+                        rec = {"R": R, "esize": es, "n": n, "units": n * es // 16, "strategy": strategy,
+                               "us": round(us, 3)}
+                        out.write(json.dumps(rec) + "\n")
+                        out.flush()
+                del big, o_big
+                torch.cuda.empty_cache()
+                print(f"swept sums R={R} {dtype}", file=sys.stderr)
+
+
+def sum_table(path: str, margin: float = 0.02):
+    """Writes kSumAutoTable: per (element size, R), the faster partition at each measured n -- the R
+    rank slices only where they beat one slice by more than `margin` (below that the two are within
+    the noise of the measurement, and one slice is kept) -- merged into ascending ranges of 16-byte
+    vectors, the last one open."""
+    times = {}
+    with open(path) as f:
+        for line in f:
+            r = json.loads(line)
+            times.setdefault((r["esize"], r["R"], r["units"]), {})[r["strategy"]] = r
+    best = {}
+    for key, t in times.items():
+        one, two = t.get("ONESHOT"), t.get("TWOSHOT")
+        best[key] = two if one is None or (two is not None and two["us"] < one["us"] * (1.0 - margin)) else one
+    groups = {}
+    for (esize, R, units), r in sorted(best.items()):
+        groups.setdefault((esize, R), []).append((units, r))
+    lines = []
+    for (esize, R), items in sorted(groups.items()):
+        items.sort()
+        code = {"ONESHOT": 1, "TWOSHOT": 2}
+        run_start = 0
+        for i, (units, r) in enumerate(items):
+            last = i + 1 == len(items)
+            if last or code[items[i + 1][1]["strategy"]] != code[r["strategy"]]:
+                umax = "9223372036854775807LL" if last else f"{units}LL"
+                first = items[run_start][0]
+                lines.append(f"    {{{esize}, {R}, {umax}, {code[r['strategy']]}}},  // {first}..{units} vectors: "
+                             f"{'one slice' if r['strategy'] == 'ONESHOT' else f'{R} rank slices'}")
+                run_start = i + 1
+    header = open(TABLE).read()
+    start = header.index("static const SumAutoEntry kSumAutoTable[] = {")
+    end = header.index("};", start)
+    body = "static const SumAutoEntry kSumAutoTable[] = {\n" + "\n".join(lines) + \
+        "\n    {0, 0, 0, 0},  // sentinel\n"
+    with open(TABLE, "w") as f:
+        f.write(header[:start] + body + header[end:])
+    print(f"wrote {len(lines)} reduce-only entries to {TABLE}")
+
+
 if __name__ == "__main__":
     cmd = sys.argv[1] if len(sys.argv) > 1 else ""
     if cmd == "_child":
@@ -204,6 +296,10 @@ if __name__ == "__main__":
               tokens=[int(t) for t in opts.get("--tokens", "").split(",") if t] or None)
     elif cmd == "table":
         table(sys.argv[2])
+    elif cmd == "sumsweep":
+        sum_sweep(sys.argv[2])
+    elif cmd == "sumtable":
+        sum_table(sys.argv[2])
     else:
         print(__doc__)
         sys.exit(2)

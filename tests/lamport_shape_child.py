@@ -12,6 +12,8 @@ import tensor_allreduce_residual_gb300 as ar
 import workloads
 from tests import tolerance as tol
 
+ar.use_test_library()   # the settings the parent puts in the environment are read by the test build only
+
 
 def check(inp, rows=None, buf=None):
     parts = [p.cuda() for p in inp.partials]
@@ -30,8 +32,8 @@ def check(inp, rows=None, buf=None):
     if inp.bias is not None:
         terms.append(inp.bias.expand(T, H).contiguous())
     terms.append(inp.residual)
-    tol.check_sum(res.cpu(), o_res, terms, inp.dtype, "residual_out")
-    tol.check_fused_out(out.cpu(), o_out, terms, inp.weight, inv, inp.dtype, H, "out")
+    tol.check_sum(res.cpu(), o_res, terms, inp.dtype, "residual_out", R=inp.R, hidden=H)
+    tol.check_fused_out(out.cpu(), o_out, terms, inp.weight, inv, inp.dtype, H, "out", R=inp.R)
 
 
 def fused(R, T, H, dtype, seed, bias=True):

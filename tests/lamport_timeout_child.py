@@ -15,12 +15,14 @@ import tensor_allreduce_residual_gb300 as ar
 import workloads
 from tests import tolerance as tol
 
+ar.use_test_library()   # the settings the parent puts in the environment are read by the test build only
+
 
 def _check(f, out, res, what):
     ro, rr, inv = oracle.residual_rmsnorm(f.partials, f.bias, f.residual, f.weight, f.eps, f.dtype)
     terms = [p.reshape(f.tokens, f.hidden) for p in f.partials] + [f.residual]
-    tol.check_sum(res.cpu(), rr, terms, f.dtype, "residual_out " + what)
-    tol.check_fused_out(out.cpu(), ro, terms, f.weight, inv, f.dtype, f.hidden, "out " + what)
+    tol.check_sum(res.cpu(), rr, terms, f.dtype, "residual_out " + what, R=f.R, hidden=f.hidden)
+    tol.check_fused_out(out.cpu(), ro, terms, f.weight, inv, f.dtype, f.hidden, "out " + what, R=f.R)
 
 
 def main():

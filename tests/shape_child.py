@@ -9,6 +9,8 @@ import tensor_allreduce_residual_gb300 as ar
 import workloads
 from tests import tolerance as tol
 
+ar.use_test_library()   # the settings the parent puts in the environment are read by the test build only
+
 
 def check(inp, rows=None):
     parts = [p.cuda() for p in inp.partials]
@@ -27,8 +29,8 @@ def check(inp, rows=None):
     if inp.bias is not None:
         terms.append(inp.bias.expand(T, H).contiguous())
     terms.append(inp.residual)
-    tol.check_sum(res.cpu(), o_res, terms, inp.dtype, "residual_out")
-    tol.check_fused_out(out.cpu(), o_out, terms, inp.weight, inv, inp.dtype, H, "out")
+    tol.check_sum(res.cpu(), o_res, terms, inp.dtype, "residual_out", R=inp.R, hidden=H)
+    tol.check_fused_out(out.cpu(), o_out, terms, inp.weight, inv, inp.dtype, H, "out", R=inp.R)
 
 
 def main():
@@ -59,8 +61,8 @@ def main():
     torch.cuda.synchronize()
     assert o.data_ptr() == ap[5].data_ptr() and r.data_ptr() == ares.data_ptr()
     terms = [p.reshape(700, 8192) for p in al.partials] + [al.bias.expand(700, 8192).contiguous(), al.residual]
-    tol.check_sum(r.cpu(), ref[1], terms, "bf16", "aliased residual_out")
-    tol.check_fused_out(o.cpu(), ref[0], terms, al.weight, ref[2], "bf16", 8192, "aliased out")
+    tol.check_sum(r.cpu(), ref[1], terms, "bf16", "aliased residual_out", R=al.R, hidden=8192)
+    tol.check_fused_out(o.cpu(), ref[0], terms, al.weight, ref[2], "bf16", 8192, "aliased out", R=al.R)
     # The norm on its own under the same shape: the register-resident kernel
     # with these units per thread, or the bulk-copy-fed kernel streaming x alone.
     for T, H, dt in [(37, 8192, "bf16"), (21, 8000, "bf16"), (9, 4096, "fp16"), (5, 1024, "fp32")]:
@@ -70,7 +72,7 @@ def main():
         got = ar.ar_rmsnorm(x.cuda(), w.cuda(), 1e-6)
         torch.cuda.synchronize()
         ref, inv = oracle.rmsnorm(x, w, 1e-6, dt)
-        tol.check_fused_out(got.cpu(), ref, [x], w, inv, dt, H, f"rmsnorm {T}x{H} {dt}")
+        tol.check_fused_out(got.cpu(), ref, [x], w, inv, dt, H, f"rmsnorm {T}x{H} {dt}", R=1)
     assert ar.ar_device_status() == ar.AR_OK, "a kernel gave up a bounded wait"
     print("shape ok")
 

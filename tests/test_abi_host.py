@@ -53,6 +53,43 @@ def test_library_exports_every_declared_symbol(L):
         assert set(_declared_functions()) <= exported
 
 
+def test_test_library_exports_the_same_symbols(L):
+    exported = {}
+    for path in (ar.LIB_PATH, ar.TEST_LIB_PATH):
+        nm = subprocess.run(["nm", "-D", "--defined-only", path], capture_output=True, text=True)
+        if nm.returncode != 0:
+            pytest.skip("nm unavailable")
+        exported[path] = set(re.findall(r"\bT (ar_\w+)", nm.stdout))
+    assert exported[ar.LIB_PATH] == exported[ar.TEST_LIB_PATH]
+
+
+_PLAN_PROBE = """
+import ctypes, sys
+sys.path.insert(0, {root!r})
+import tensor_allreduce_residual_gb300 as ar
+if sys.argv[1] == "test":
+    ar.use_test_library()
+print(ar.ar_query_launch(8, 8192, 8192, ar.AR_BF16, "ONESHOT")["kernel_name"],
+      ar.ar_query_launch(8, 8192, 8192, ar.AR_BF16, "ONESHOT")["units_per_thread"])
+"""
+
+
+@pytest.mark.parametrize("which", ["product", "test"])
+def test_only_the_test_library_reads_the_shape_override(L, which):
+    """libar.so reads no environment variable: a launch-shape override left in the environment changes
+    nothing there.  libar_test.so applies it (the shape sweeps and the forced-shape tests rely on that)."""
+    env = dict(os.environ, AR_ONESHOT_SHAPE="1:0:1", AR_TEST_STALL_STAGE="1", AR_PDL="0")
+    res = subprocess.run(["python", "-c", _PLAN_PROBE.format(root=ROOT), which], env=env, capture_output=True,
+                         text=True, check=True)
+    kernel, vpt = res.stdout.split()
+    plain = subprocess.run(["python", "-c", _PLAN_PROBE.format(root=ROOT), "product"], capture_output=True,
+                           text=True, check=True, env={k: v for k, v in os.environ.items() if not k.startswith("AR_")})
+    if which == "product":
+        assert res.stdout == plain.stdout          # the same plan as with a clean environment
+    else:
+        assert (kernel, vpt) == ("k_fused_oneshot", "1")   # the forced register shape, one vector a thread
+
+
 def test_version_and_strerror(L):
     assert ar.ar_version() == 10000
     for code in (ar.AR_OK, ar.AR_ERR_INVALID_ARG, ar.AR_ERR_UNSUPPORTED, ar.AR_ERR_WORKSPACE, ar.AR_ERR_CUDA,

@@ -121,3 +121,47 @@ def test_sweep_skips_a_shape_that_does_not_fit():
     staged = dict(base, kernel=2, units_per_thread=4, early_residual=0, blocks_per_sm=0, stages=0)
     assert tune.shape_taken(staged, "4:1:0") and tune.shape_taken(staged, "4:2:0")   # persistent -> staged
     assert not tune.shape_taken(dict(staged, strategy=2, kernel=5), "4:1:0")
+
+
+SUM_ENTRY = re.compile(r"^\s*\{(\d+), (\d+), (\d+)LL, (\d+)\},")
+LLONG_MAX = 2 ** 63 - 1
+
+
+def sum_entries(text):
+    return [tuple(int(x) for x in m.groups()) for m in map(SUM_ENTRY.match, text.splitlines()) if m]
+
+
+def test_sum_table_from_a_sweep(tmp_path, monkeypatch):
+    """The faster partition per measured n, rank slices only beyond the noise margin, merged into ranges."""
+    table = tmp_path / "ar_auto_table.h"
+    shutil.copy(tune.TABLE, table)
+    monkeypatch.setattr(tune, "TABLE", str(table))
+    recs = []
+    for units, one, two in [(64, 1.70, 1.60), (128, 1.80, 1.62), (256, 2.00, 1.99), (512, 2.20, 2.30),
+                            (1024, 3.00, 2.50), (2048, 5.0, 5.2)]:
+        recs += [dict(R=4, esize=2, n=units * 8, units=units, strategy="ONESHOT", us=one),
+                 dict(R=4, esize=2, n=units * 8, units=units, strategy="TWOSHOT", us=two)]
+    sweep = tmp_path / "sums.jsonl"
+    sweep.write_text("".join(json.dumps(r) + "\n" for r in recs))
+    tune.sum_table(str(sweep))
+    assert sum_entries(table.read_text()) == [
+        (2, 4, 128, 2),        # rank slices clearly faster up to 128 vectors
+        (2, 4, 512, 1),        # within 2 % at 256 (one slice kept), slower at 512
+        (2, 4, 1024, 2),
+        (2, 4, LLONG_MAX, 1),  # the last range is open
+    ]
+    # the fused table is untouched
+    assert entries(table.read_text()) == entries(open(tune.TABLE).read())
+
+
+def test_reduce_only_auto_is_the_table_choice(L):
+    """ar_query_strategy(..., AR_FUSION_NONE) reports, at every measured size of every committed entry
+    range, the partition the table names (AUTO in ar_sum takes the same function)."""
+    rows = sum_entries(open(tune.TABLE).read())
+    for esize, R, umax, strategy in rows:
+        dtype = ar.AR_FP16 if esize == 2 else ar.AR_FP32
+        lanes = 16 // esize
+        lo = max([u for e, r, u, _ in rows if e == esize and r == R and u < umax], default=0)
+        for units in {lo + 1, min(umax, 1 << 26)}:
+            s, _ = ar.ar_query_strategy(R, units * lanes, 0, dtype, ar.AR_FUSION_NONE)
+            assert s == strategy, (esize, R, units, s, strategy)

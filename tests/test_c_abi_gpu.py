@@ -46,8 +46,8 @@ def test_c_program_through_the_abi(tmp_path):
     got = torch.from_numpy(np.fromfile(outp, dtype=np.float32)).reshape(5, T, H)
     ref_out, ref_res, inv = oracle.residual_rmsnorm(f.partials, f.bias, f.residual, f.weight, EPS, "fp32")
     terms = [p.reshape(T, H) for p in f.partials] + [f.bias.expand(T, H).contiguous(), f.residual]
-    tol.check_sum(got[1], ref_res, terms, "fp32", "residual_out")
-    tol.check_fused_out(got[0], ref_out, terms, f.weight, inv, "fp32", H, "out")
-    tol.check_sum(got[2], oracle.sum(f.partials, "fp32"), f.partials, "fp32", "sum")
-    tol.check_sum(got[4], ref_res, terms, "fp32", "Lamport residual_out")
-    tol.check_fused_out(got[3], ref_out, terms, f.weight, inv, "fp32", H, "Lamport out")
+    tol.check_sum(got[1], ref_res, terms, "fp32", "residual_out", R=f.R, hidden=H)
+    tol.check_fused_out(got[0], ref_out, terms, f.weight, inv, "fp32", H, "out", R=f.R)
+    tol.check_sum(got[2], oracle.sum(f.partials, "fp32"), f.partials, "fp32", "sum", R=f.R)
+    tol.check_sum(got[4], ref_res, terms, "fp32", "Lamport residual_out", R=f.R, hidden=H)
+    tol.check_fused_out(got[3], ref_out, terms, f.weight, inv, "fp32", H, "Lamport out", R=f.R)

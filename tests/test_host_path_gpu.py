@@ -44,8 +44,8 @@ def _check(inp, out, rout):
     if inp.bias is not None:
         terms.append(inp.bias.expand(inp.tokens, inp.hidden).contiguous())
     terms.append(inp.residual)
-    tol.check_sum(rout, ref[1], terms, inp.dtype, "residual_out")
-    tol.check_fused_out(out, ref[0], terms, inp.weight, ref[2], inp.dtype, inp.hidden, "out")
+    tol.check_sum(rout, ref[1], terms, inp.dtype, "residual_out", R=inp.R, hidden=inp.hidden)
+    tol.check_fused_out(out, ref[0], terms, inp.weight, ref[2], inp.dtype, inp.hidden, "out", R=inp.R)
     d_out, d_rout = ar.ar_residual_rmsnorm([p.cuda() for p in inp.partials], inp.residual.cuda(), inp.weight.cuda(),
                                            inp.eps, bias=None if inp.bias is None else inp.bias.cuda())
     assert torch.equal(d_rout.cpu().view(torch.uint8), rout.view(torch.uint8))

@@ -54,8 +54,8 @@ def check(inp, out, res, what=""):
     o_out, o_res, inv = oracle.residual_rmsnorm(inp.partials, inp.bias, inp.residual, inp.weight, inp.eps,
                                                 inp.dtype)
     terms = terms_of(inp)
-    tol.check_sum(res, o_res, terms, inp.dtype, "residual_out " + what)
-    tol.check_fused_out(out, o_out, terms, inp.weight, inv, inp.dtype, inp.hidden, "out " + what)
+    tol.check_sum(res, o_res, terms, inp.dtype, "residual_out " + what, R=inp.R, hidden=inp.hidden)
+    tol.check_fused_out(out, o_out, terms, inp.weight, inv, inp.dtype, inp.hidden, "out " + what, R=inp.R)
 
 
 def all_marker(buf, dtype, nbytes):

@@ -64,8 +64,8 @@ def check_fused(inp, out, res, ref=None):
         ref = oracle.residual_rmsnorm(inp.partials, inp.bias, inp.residual, inp.weight, inp.eps, inp.dtype)
     o_out, o_res, inv = ref
     terms = terms_of(inp)
-    r1 = tol.check_sum(res, o_res, terms, inp.dtype, "residual_out")
-    r2 = tol.check_fused_out(out, o_out, terms, inp.weight, inv, inp.dtype, inp.hidden, "out")
+    r1 = tol.check_sum(res, o_res, terms, inp.dtype, "residual_out", R=inp.R, hidden=inp.hidden)
+    r2 = tol.check_fused_out(out, o_out, terms, inp.weight, inv, inp.dtype, inp.hidden, "out", R=inp.R)
     return r1, r2
 
 
@@ -92,7 +92,7 @@ def test_pr1_fused_and_sum(strategy):
     out, res = run_fused(inp, strategy)
     check_fused(inp, out, res)
     s = ar.ar_sum([dev(p) for p in inp.partials], strategy=strategy).cpu()
-    tol.check_sum(s, oracle.sum(inp.partials, "fp32"), inp.partials, "fp32")
+    tol.check_sum(s, oracle.sum(inp.partials, "fp32"), inp.partials, "fp32", R=inp.R)
 
 
 def test_tp_decode_all_token_counts():
@@ -117,7 +117,7 @@ def test_reduce_only_full_compare(n):
     outs = []
     for strategy in STRATS:
         s = ar.ar_sum([dev(p) for p in inp.partials], strategy=strategy).cpu()
-        tol.check_sum(s, ref, inp.partials, "fp16")
+        tol.check_sum(s, ref, inp.partials, "fp16", R=inp.R)
         outs.append(s)
     assert all(torch.equal(bits(outs[0]), bits(o)) for o in outs[1:])
 
@@ -136,7 +136,7 @@ def test_reduce_only_large_sampled(n):
         outs.append(s[idx.cuda()].cpu())
         del s
     for o in outs:
-        tol.check_sum(o, ref, [p[idx] for p in inp.partials], "fp16")
+        tol.check_sum(o, ref, [p[idx] for p in inp.partials], "fp16", R=inp.R)
     assert all(torch.equal(bits(outs[0]), bits(o)) for o in outs[1:])
 
 
@@ -189,7 +189,7 @@ def test_sum_ragged_sizes_and_rank_counts(dtype, R):
         ref = oracle.sum(inp.partials, dtype)
         outs = [ar.ar_sum([dev(p) for p in inp.partials], strategy=s).cpu() for s in STRATS]
         for o in outs:
-            tol.check_sum(o, ref, inp.partials, dtype)
+            tol.check_sum(o, ref, inp.partials, dtype, R=R)
             assert torch.equal(bits(outs[0]), bits(o))
 
 
@@ -231,7 +231,7 @@ def test_misaligned_pointers_take_the_elementwise_path(dtype):
     parts = [_offset_view(p, 1 + r % 3) for r, p in enumerate(inp.partials)]
     out = _offset_view(torch.zeros(10007, dtype=TD[dtype]), 2)
     ar.ar_sum(parts, out=out)
-    tol.check_sum(out.cpu(), ref, inp.partials, dtype)
+    tol.check_sum(out.cpu(), ref, inp.partials, dtype, R=inp.R)
 
     f = workloads.fused_inputs(2, 9, 256, dtype, partial_dist=("N", 0.0, 0.5), residual_dist=("N", 0.0, 4.0),
                                bias_dist=("N", 0.0, 0.02), weight_dist=("N", 1.0, 0.05), eps=1e-6, seed=4)
@@ -296,7 +296,7 @@ def test_aliasing_out_on_partial_and_residual_out_on_residual(strategy):
     ref_s = oracle.sum(s_in.partials, "fp16")
     sp = [dev(p) for p in s_in.partials]
     ar.ar_sum(sp, out=sp[0], strategy=strategy)
-    tol.check_sum(sp[0].cpu(), ref_s, s_in.partials, "fp16")
+    tol.check_sum(sp[0].cpu(), ref_s, s_in.partials, "fp16", R=s_in.R)
 
 
 def test_determinism_across_runs_and_strategies():
@@ -395,7 +395,7 @@ def test_rmsnorm_matches_oracle(dtype, T, H):
     out = ar.ar_rmsnorm(x.cuda(), w.cuda(), eps)
     torch.cuda.synchronize()
     ref, inv = oracle.rmsnorm(x, w, eps, dtype)
-    tol.check_fused_out(out.cpu(), ref, [x], w, inv, dtype, H, "rmsnorm out")
+    tol.check_fused_out(out.cpu(), ref, [x], w, inv, dtype, H, "rmsnorm out", R=1)
 
 
 def test_rmsnorm_in_place_and_limits():
@@ -405,7 +405,8 @@ def test_rmsnorm_in_place_and_limits():
     ar.ar_rmsnorm(xd, w.cuda(), 1e-6, out=xd)
     torch.cuda.synchronize()
     assert torch.equal(xd.cpu().view(torch.int16), ar.ar_rmsnorm(x.cuda(), w.cuda(), 1e-6).cpu().view(torch.int16))
-    tol.check_fused_out(xd.cpu(), ref, [x], w, oracle.rmsnorm(x, w, 1e-6, "bf16")[1], "bf16", 8192, "in place")
+    tol.check_fused_out(xd.cpu(), ref, [x], w, oracle.rmsnorm(x, w, 1e-6, "bf16")[1], "bf16", 8192, "in place",
+                        R=1)
     big = torch.zeros(1, 16385, dtype=torch.bfloat16, device="cuda")
     with pytest.raises(ar.ARError) as e:
         ar.ar_rmsnorm(big, torch.ones(16385, dtype=torch.bfloat16, device="cuda"), 1e-6)
@@ -423,7 +424,7 @@ def test_unfused_route_matches_oracle_composition(dtype, R, T, H, has_bias):
     out, res = ar.ar_residual_rmsnorm([s], dev(inp.residual), dev(inp.weight), inp.eps, bias=dev(inp.bias))
     torch.cuda.synchronize()
     s_ref = oracle.sum(inp.partials, dtype)
-    tol.check_sum(s.cpu(), s_ref, [p.reshape(T, H) for p in inp.partials], dtype, "sum")
+    tol.check_sum(s.cpu(), s_ref, [p.reshape(T, H) for p in inp.partials], dtype, "sum", R=R)
     step2 = workloads.FusedInputs(1, T, H, dtype, inp.eps, [s_ref.reshape(T, H)], inp.residual, inp.weight, inp.bias)
     check_fused(step2, out.cpu(), res.cpu())
 
@@ -458,7 +459,8 @@ def test_allreduce_config_flags_match_allreduce(config, strategy):
     if fused:
         check_fused(f, *outs[1])
     else:
-        tol.check_sum(outs[1][0], oracle.sum(f.partials, "bf16"), [q.reshape(33, 8192) for q in f.partials], "bf16")
+        tol.check_sum(outs[1][0], oracle.sum(f.partials, "bf16"), [q.reshape(33, 8192) for q in f.partials], "bf16",
+                      R=f.R)
 
 
 @pytest.mark.parametrize("R,dtype,H,T", [(16, "bf16", 8192, 5), (16, "bf16", 8192, 64), (16, "bf16", 8192, 300),

@@ -71,17 +71,17 @@ def test_random_shape_matches_oracle(R, dt, H, T, has_bias, strategy, seed):
     if f.bias is not None:
         terms.append(f.bias.expand(T, H).contiguous())
     terms.append(f.residual)
-    tol.check_sum(res.cpu(), ref_res, terms, dt, "residual_out")
-    tol.check_fused_out(out.cpu(), ref_out, terms, f.weight, inv, dt, H, "out")
+    tol.check_sum(res.cpu(), ref_res, terms, dt, "residual_out", R=R, hidden=H)
+    tol.check_fused_out(out.cpu(), ref_out, terms, f.weight, inv, dt, H, "out", R=R)
     # and the plain sum of the same partials
     s = ar.ar_sum(parts, strategy="TWOSHOT" if strategy == "TWOSHOT" else "ONESHOT")
     torch.cuda.synchronize()
-    tol.check_sum(s.cpu(), oracle.sum(f.partials, dt), f.partials, dt, "sum")
+    tol.check_sum(s.cpu(), oracle.sum(f.partials, dt), f.partials, dt, "sum", R=R)
     # and the Lamport-style call, wherever it takes the shape
     if ar.ar_lamport_supported(R, H, T, workloads.DTYPES[dt]) is not None:
         lo, lr = ar.ar_residual_rmsnorm_lamport(parts, f.residual.cuda(), f.weight.cuda(), f.eps,
                                                 bias=None if f.bias is None else f.bias.cuda())
         torch.cuda.synchronize()
-        tol.check_sum(lr.cpu(), ref_res, terms, dt, "Lamport residual_out")
-        tol.check_fused_out(lo.cpu(), ref_out, terms, f.weight, inv, dt, H, "Lamport out")
+        tol.check_sum(lr.cpu(), ref_res, terms, dt, "Lamport residual_out", R=R, hidden=H)
+        tol.check_fused_out(lo.cpu(), ref_out, terms, f.weight, inv, dt, H, "Lamport out", R=R)
         assert ar.ar_device_status() == ar.AR_OK
