@@ -87,6 +87,52 @@ struct SumAutoEntry {
 };
 
 static const SumAutoEntry kSumAutoTable[] = {
+    {2, 2, 2048LL, 2},  // 64..2048 vectors: 2 rank slices
+    {2, 2, 524288LL, 1},  // 4096..524288 vectors: one slice
+    {2, 2, 1048576LL, 2},  // 1048576..1048576 vectors: 2 rank slices
+    {2, 2, 9223372036854775807LL, 1},  // 2097152..16777216 vectors: one slice
+    {2, 3, 128LL, 1},  // 64..128 vectors: one slice
+    {2, 3, 4096LL, 2},  // 256..4096 vectors: 3 rank slices
+    {2, 3, 9223372036854775807LL, 1},  // 8192..16777216 vectors: one slice
+    {2, 4, 64LL, 1},  // 64..64 vectors: one slice
+    {2, 4, 2048LL, 2},  // 128..2048 vectors: 4 rank slices
+    {2, 4, 262144LL, 1},  // 4096..262144 vectors: one slice
+    {2, 4, 524288LL, 2},  // 524288..524288 vectors: 4 rank slices
+    {2, 4, 9223372036854775807LL, 1},  // 1048576..16777216 vectors: one slice
+    {2, 8, 128LL, 1},  // 64..128 vectors: one slice
+    {2, 8, 2048LL, 2},  // 256..2048 vectors: 8 rank slices
+    {2, 8, 32768LL, 1},  // 4096..32768 vectors: one slice
+    {2, 8, 65536LL, 2},  // 65536..65536 vectors: 8 rank slices
+    {2, 8, 9223372036854775807LL, 1},  // 131072..16777216 vectors: one slice
+    {2, 16, 128LL, 1},  // 64..128 vectors: one slice
+    {2, 16, 16384LL, 2},  // 256..16384 vectors: 16 rank slices
+    {2, 16, 9223372036854775807LL, 1},  // 32768..16777216 vectors: one slice
+    {4, 2, 128LL, 2},  // 128..128 vectors: 2 rank slices
+    {4, 2, 256LL, 1},  // 256..256 vectors: one slice
+    {4, 2, 2048LL, 2},  // 512..2048 vectors: 2 rank slices
+    {4, 2, 16384LL, 1},  // 4096..16384 vectors: one slice
+    {4, 2, 65536LL, 2},  // 32768..65536 vectors: 2 rank slices
+    {4, 2, 131072LL, 1},  // 131072..131072 vectors: one slice
+    {4, 2, 262144LL, 2},  // 262144..262144 vectors: 2 rank slices
+    {4, 2, 524288LL, 1},  // 524288..524288 vectors: one slice
+    {4, 2, 1048576LL, 2},  // 1048576..1048576 vectors: 2 rank slices
+    {4, 2, 9223372036854775807LL, 1},  // 2097152..33554432 vectors: one slice
+    {4, 3, 128LL, 1},  // 128..128 vectors: one slice
+    {4, 3, 4096LL, 2},  // 256..4096 vectors: 3 rank slices
+    {4, 3, 262144LL, 1},  // 8192..262144 vectors: one slice
+    {4, 3, 524288LL, 2},  // 524288..524288 vectors: 3 rank slices
+    {4, 3, 9223372036854775807LL, 1},  // 1048576..33554432 vectors: one slice
+    {4, 4, 2048LL, 2},  // 128..2048 vectors: 4 rank slices
+    {4, 4, 9223372036854775807LL, 1},  // 4096..33554432 vectors: one slice
+    {4, 8, 2048LL, 2},  // 128..2048 vectors: 8 rank slices
+    {4, 8, 65536LL, 1},  // 4096..65536 vectors: one slice
+    {4, 8, 131072LL, 2},  // 131072..131072 vectors: 8 rank slices
+    {4, 8, 524288LL, 1},  // 262144..524288 vectors: one slice
+    {4, 8, 1048576LL, 2},  // 1048576..1048576 vectors: 8 rank slices
+    {4, 8, 9223372036854775807LL, 1},  // 2097152..33554432 vectors: one slice
+    {4, 16, 256LL, 1},  // 128..256 vectors: one slice
+    {4, 16, 8192LL, 2},  // 512..8192 vectors: 16 rank slices
+    {4, 16, 9223372036854775807LL, 1},  // 16384..33554432 vectors: one slice
     {0, 0, 0, 0},  // sentinel
 };
 
