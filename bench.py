@@ -385,6 +385,30 @@ def _time_graph(torch, fn, n=20, reps=5):
     return statistics.median(ts)
 
 
+def _time_graph_precise(torch, fn, nbytes):
+    """Median over 11 replays of a graph of up to 100 calls (about 20 ms of work per replay at most)."""
+    est_us = nbytes / 6.5e3 + 2.0
+    return _time_graph(torch, fn, n=max(3, min(100, int(20000 / est_us))), reps=11)
+
+
+def _time_rotate(torch, fns, stream, rounds=10):
+    """Mean device time per call of back-to-back calls that cycle through `fns`, each on its own inputs:
+    with the input sets together several times the size of L2, every call finds its inputs evicted by
+    the others (L2-cold inputs, no flush between calls, launches overlapped as in a stream of layers)."""
+    for f in fns:
+        f()
+    torch.cuda.synchronize()
+    torch.cuda._sleep(50000)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(rounds):
+        for f in fns:
+            f()
+    b.record(stream)
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) / (rounds * len(fns))
+
+
 def run_extras(ar, torch, workloads, parts, resid, weight, bias, out, res_out, ws, bytes_call, stream):
     """Secondary numbers: each fixed strategy on the prefill inputs, decode latency, reduce-only bandwidth.
 
@@ -400,17 +424,18 @@ def run_extras(ar, torch, workloads, parts, resid, weight, bias, out, res_out, w
             parts, resid, weight, EPS, bias=bias, out=out, residual_out=res_out, intermediate=ws,
             strategy=s), stream, 100)
         ex[f"prefill_{s}"] = {"us_per_call": round(ms * 1e3, 2), "GBps": round(bytes_call / ms / 1e6, 1)}
-    # The Lamport-style call on the same inputs: its buffer is written, read
-    # and emptied again, 3 R n s bytes beyond the fused call's (GBps counts the
-    # fused call's bytes, GBps_protocol all of them).
+    # The Lamport-style call on the same inputs.  Its buffer (a ring of two
+    # grid steps of rows) is written, read and emptied through L2: 3 R n s
+    # bytes beyond the fused call's pass there, not through DRAM.  GBps and
+    # frac count the fused call's algorithmic bytes.
     T0, H0 = resid.shape
     lam = ar.lamport_buffer(len(parts), H0, T0, resid.dtype, resid.device)
     ms = _time_calls(torch, lambda: ar.ar_residual_rmsnorm_lamport(parts, resid, weight, EPS, bias=bias, out=out,
                                                                    residual_out=res_out, buffer=lam), stream, 30)
-    extra = 3 * len(parts) * T0 * H0 * resid.element_size()
+    peak0, _ = measured_peaks()
     ex["prefill_LAMPORT"] = {"us_per_call": round(ms * 1e3, 2), "GBps": round(bytes_call / ms / 1e6, 1),
-                             "protocol_bytes": bytes_call + extra,
-                             "GBps_protocol": round((bytes_call + extra) / ms / 1e6, 1),
+                             "frac_of_peak": round(bytes_call / ms / 1e6 / peak0, 4),
+                             "buffer_bytes": lam.numel(),
                              "over_oneshot": round(ms * 1e3 / ex["prefill_ONESHOT"]["us_per_call"], 3)}
     del lam
     # The unfused route (the pages' "all-reduce, then norm"): ar_sum into a
@@ -451,25 +476,47 @@ def run_extras(ar, torch, workloads, parts, resid, weight, bias, out, res_out, w
     flush = (torch.empty(256 << 20, dtype=torch.uint8, device="cuda"),
              torch.zeros(256 << 20, dtype=torch.uint8, device="cuda"))
     # The prefill curve: R=8 bf16 H=8192 at 512 .. 4096 tokens (90 .. 738 MB
-    # a call) through AUTO.  Cold: L2 flushed before each call, mean of 20;
-    # warm: back-to-back calls.
+    # a call) through AUTO.  Cold: each call alone after an L2 flush, mean of
+    # 20 (launch latency and the cold start of an isolated call included).
+    # Cold stream: back to back on input sets that together exceed L2 several
+    # times, so every call's inputs come from DRAM.  Warm: back-to-back calls
+    # on the same inputs.  copy_us_cold: a plain device copy of the same
+    # number of bytes timed like `cold`; read_same_bytes_us_cold: a read-only
+    # pass (a sum) over as many bytes as the call reads (its 9 inputs), timed
+    # the same way -- the floors that this way of timing sets at each size
+    # (an isolated launch between events costs about 4 us here by itself).
     peak, _ = measured_peaks()
     curve = {}
     for T in (512, 1024, 2048, 4096):
-        f = workloads.tp_prefill(tokens=T, device="cuda")
-        o, r = torch.empty_like(f.residual), torch.empty_like(f.residual)
-        wT = torch.empty(ar.ar_workspace_size_rows(8, 8192, T, ar.AR_BF16), dtype=torch.uint8, device="cuda")
-        fn = lambda f=f, o=o, r=r, wT=wT: ar.ar_residual_rmsnorm(  # noqa: E731
-            f.partials, f.residual, f.weight, f.eps, bias=f.bias, out=o, residual_out=r, intermediate=wT,
-            strategy="AUTO")
         b = algorithmic_bytes(8, T, 8192, 2, has_bias=True)
-        cold = _time_cold(torch, fn, stream, flush, 20)
-        warm = _time_calls(torch, fn, stream, 50)
+        nsets = max(2, -(-400_000_000 // b))
+        sets = []
+        for k in range(nsets):
+            f = workloads.tp_prefill(tokens=T, seed=k, device="cuda")
+            o, r = torch.empty_like(f.residual), torch.empty_like(f.residual)
+            wT = torch.empty(ar.ar_workspace_size_rows(8, 8192, T, ar.AR_BF16), dtype=torch.uint8, device="cuda")
+            sets.append((f, o, r, wT))
+        fns = [lambda f=f, o=o, r=r, wT=wT: ar.ar_residual_rmsnorm(
+            f.partials, f.residual, f.weight, f.eps, bias=f.bias, out=o, residual_out=r, intermediate=wT,
+            strategy="AUTO") for f, o, r, wT in sets]
+        cold = _time_cold(torch, fns[0], stream, flush, 20)
+        cold_stream = _time_rotate(torch, fns, stream)
+        warm = _time_calls(torch, fns[0], stream, 50)
+        src = torch.empty(b // 2, dtype=torch.uint8, device="cuda")
+        dst = torch.empty_like(src)
+        copy_cold = _time_cold(torch, lambda: dst.copy_(src), stream, flush, 20)
+        reads = torch.zeros(9 * T * 8192 // 2, dtype=torch.float32, device="cuda")
+        read_cold = _time_cold(torch, lambda: reads.sum(), stream, flush, 20)
         curve[f"T{T}"] = {"bytes": b, "kernel": ar.ar_query_launch(8, 8192, T, ar.AR_BF16, "AUTO")["kernel_name"],
                           "us_cold": round(cold * 1e3, 2), "GBps_cold": round(b / cold / 1e6, 1),
                           "frac_cold": round(b / cold / 1e6 / peak, 4),
-                          "us_warm": round(warm * 1e3, 2), "GBps_warm": round(b / warm / 1e6, 1)}
-        del f, o, r, wT
+                          "us_cold_stream": round(cold_stream * 1e3, 2),
+                          "frac_cold_stream": round(b / cold_stream / 1e6 / peak, 4),
+                          "us_warm": round(warm * 1e3, 2), "GBps_warm": round(b / warm / 1e6, 1),
+                          "copy_us_cold": round(copy_cold * 1e3, 2),
+                          "copy_frac_cold": round(b / copy_cold / 1e6 / peak, 4),
+                          "read_same_bytes_us_cold": round(read_cold * 1e3, 2)}
+        del sets, fns, src, dst, reads
     ex["prefill_curve_R8_bf16_H8192_AUTO"] = curve
     # PR1 reference case: R=2 fp32, 4 x 64, fusion NONE and RESIDUAL_RMS_NORM.
     p1 = workloads.pr1(seed=0)
@@ -527,9 +574,13 @@ def run_extras(ar, torch, workloads, parts, resid, weight, bias, out, res_out, w
     for v in r8.values():   # AUTO against the better fixed strategy (graph replay)
         v["auto_over_best_fixed"] = round(v["us_graph"] / min(v["us_graph_oneshot"], v["us_graph_twoshot"]), 3)
     ex["decode_R8_bf16_H8192"] = r8
-    del flush
     # Reduce-only sweep, R=4 fp16, n = 2^9 .. 2^27: device time per call
-    # (graph replay).  Working sets below L2 (129 MB) are partly served by L2.
+    # from a replayed graph of up to 100 calls, median of 11 replays (about
+    # 0.01 us of resolution at the smallest sizes; working sets below L2,
+    # 129 MB, are served partly by L2), each fixed partition and AUTO, with
+    # AUTO's ratio to the better fixed one.  From 2^23 (84 MB) up also
+    # L2-cold: each call alone after an L2 flush (`us_cold`), and back to back
+    # on input sets that together exceed L2 several times (`us_cold_stream`).
     red = {}
     big = workloads.reduce_only(1 << 27, device="cuda")
     o_big = torch.empty_like(big.partials[0])
@@ -540,10 +591,27 @@ def run_extras(ar, torch, workloads, parts, resid, weight, bias, out, res_out, w
         b = workloads.sum_algorithmic_bytes(4, n, "fp16")
         row = {}
         for s in ("ONESHOT", "TWOSHOT", "AUTO"):
-            ms = _time_graph(torch, lambda s=s: ar.ar_sum(parts_n, out=o, strategy=s), n=10, reps=3)
-            row[s] = {"us": round(ms * 1e3, 2), "GBps": round(b / ms / 1e6, 1)}
+            ms = _time_graph_precise(torch, lambda s=s: ar.ar_sum(parts_n, out=o, strategy=s), b)
+            row[s] = {"us": round(ms * 1e3, 3), "GBps": round(b / ms / 1e6, 1)}
+        row["auto"] = ar.STRATEGY_NAMES[ar.ar_query_strategy(4, n, 0, ar.AR_FP16, ar.AR_FUSION_NONE)[0]]
+        row["auto_over_best_fixed"] = round(row["AUTO"]["us"] / min(row["ONESHOT"]["us"], row["TWOSHOT"]["us"]), 3)
+        if k >= 23:
+            sets = [(parts_n, o)] + [([torch.empty_like(p) for p in parts_n], torch.empty_like(o))
+                                     for _ in range(max(1, -(-400_000_000 // b)) - 1)]
+            for ps, _ in sets[1:]:
+                for p, q in zip(ps, parts_n):
+                    p.copy_(q)
+            cold = _time_cold(torch, lambda: ar.ar_sum(parts_n, out=o, strategy="AUTO"), stream, flush, 20)
+            fns = [lambda ps=ps, oo=oo: ar.ar_sum(ps, out=oo, strategy="AUTO") for ps, oo in sets]
+            stream_cold = _time_rotate(torch, fns, stream)
+            row["us_cold"] = round(cold * 1e3, 2)
+            row["frac_cold"] = round(b / cold / 1e6 / peak, 4)
+            row["us_cold_stream"] = round(stream_cold * 1e3, 2)
+            row["frac_cold_stream"] = round(b / stream_cold / 1e6 / peak, 4)
+            del sets, fns
         red[f"2^{k}"] = row
     ex["reduce_only_R4_fp16_sweep"] = red
+    del flush
     # R=1 (the tpSize=1 passthrough): a copy into another buffer, and the
     # in-place call, which launches nothing.
     src = big.partials[0]

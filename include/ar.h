@@ -426,23 +426,32 @@ int ar_residual_rmsnorm_noalloc(const void* const* partials, int R, const void* 
  * by other blocks), so the call reads the R partials like the other fused
  * calls and returns the same out and residual_out, except that an element
  * of residual_out or out that is an exact zero may have the other sign.
- * On one GPU it moves more bytes than the one-shot call (the buffer is
- * written, read and emptied: 3 * R * tokens * hidden elements more), and
- * it is provided for the protocol, not for speed.
+ * On one GPU it moves more bytes through L2 than the one-shot call (the
+ * buffer is written, read and emptied: 3 * R * tokens * hidden elements
+ * more), and it is provided for the protocol, not for speed.
  *
- * Buffer layout: slot r = [tokens][hidden] elements at offset
- *   r * tokens * hidden * element size; ar_lamport_buffer_size gives the
- *   bytes.  The buffer is caller-owned device memory, 16-byte aligned, and
- *   must hold the marker everywhere before a call: fill it once with
- *   ar_lamport_init; every call that completes leaves it that way.  A buffer
- *   filled for one element type serves calls of that type only (the fp32
- *   and 16-bit markers differ).  Calls that share a buffer must be ordered
- *   (one stream, or events).
+ * Buffer layout: 4096 bytes of progress words (one per block of the
+ *   launch: they tell a block when a ring row has been emptied), then slot
+ *   r = [slot_rows][hidden] elements at offset 4096 + r * slot_rows * hidden
+ *   * element size, then 64 bytes per token of exchange area for rows split
+ *   over several blocks.  The slots are a ring:
+ *   row k of a call uses ring row k mod ring_rows, where ring_rows (at most
+ *   slot_rows) covers two steps of the launch's row groups, so a slot holds
+ *   at most 1024 row groups (one to several rows each, by the launch shape)
+ *   however many tokens the call has; a row beyond the ring waits for its
+ *   ring row to be emptied by the reduce of the row before it.
+ *   ar_lamport_buffer_size gives the bytes.  The buffer is caller-owned
+ *   device memory, 16-byte aligned, and must hold the marker everywhere
+ *   before its first call: fill it once with ar_lamport_init; every call
+ *   that completes leaves its slots and exchange area that way (the progress
+ *   words it leaves are never mistaken for a later call's).  A buffer filled for one element type
+ *   serves calls of that type only (the fp32 and 16-bit markers differ).
+ *   Calls that share a buffer must be ordered (one stream, or events).
  */
 
 /* Bytes of the Lamport buffer for R partials of [tokens, hidden] elements
- * (R * tokens * hidden * element size, rounded up to 256); 0 for bad
- * arguments. */
+ * (the R ring slots and the exchange area, rounded up to 256); 0 for bad
+ * arguments or a shape the call cannot take (ar_lamport_supported). */
 size_t ar_lamport_buffer_size(int R, int hidden, int tokens, int dtype);
 
 /*
@@ -499,6 +508,80 @@ int ar_residual_rmsnorm_lamport(const void* const* partials, int R, const void* 
                                 int hidden, int tokens, void* out, void* residual_out,
                                 void* lamport_buffer, size_t lamport_bytes, int dtype,
                                 ar_stream_t stream);
+
+/*
+ * ---------------------------------------------------------------------------
+ * The all-reduce across the GPUs of one node: one process (rank) per GPU,
+ * every rank's partial in its own GPU's memory, each rank reading its peers'
+ * registered buffers directly (AllReduceParams::peer_comm_buffer_ptrs
+ * [MAX_RANKS_PER_NODE], "type.d2"; oneShotAllReduceKernel and
+ * twoShotAllReduceKernel with their block barriers, "allreduce.d2").  Every
+ * rank gets out = sum over ranks of each rank's input, accumulated in fp32 in
+ * rank order (the same values on every rank, and the same values as ar_sum
+ * over the R inputs).
+ *
+ * Set-up, on every rank: allocate (cudaMalloc, or a caching allocator's
+ * device memory) ar_comm_buffer_size(world, max_bytes) bytes, export its IPC
+ * handle with ar_comm_export, exchange the handles among the ranks (any
+ * host-side channel: the Python binding uses torch.distributed), call
+ * ar_comm_create with all of them in rank order, then pass a host-side
+ * barrier among the ranks before the first ar_allreduce_peer: create zeroes
+ * this rank's flag words, and no peer may signal into them before that.
+ * Every rank must then make the same sequence of calls (same n, dtype and
+ * strategy).  With world == 1 no handle is needed (handles may be NULL).
+ *
+ * Waits: every block barrier gives up after one second (a rank that never
+ * arrives); the kernel then finishes without the missing data, the event is
+ * recorded for ar_device_status (AR_ERR_TIMEOUT) and out is incomplete.
+ * Plain peer loads and stores over NVLink; no multicast.  Not measured on more
+ * than one GPU: every box this library was built and tested on has one
+ * (world == 1 runs the same kernels, barrier included).
+ * ---------------------------------------------------------------------------
+ */
+#define AR_IPC_HANDLE_BYTES 64
+typedef struct ar_comm ar_comm;
+
+/* Bytes each rank registers: 16 KiB of flag words plus two data areas of
+ * max_bytes (rounded up to 256); 0 for bad arguments. */
+size_t ar_comm_buffer_size(int world, size_t max_bytes);
+
+/* Writes the AR_IPC_HANDLE_BYTES-byte CUDA IPC handle of `buffer` (device
+ * memory of the current device, the start of an allocation) to `handle`
+ * (host memory).  Errors: AR_ERR_INVALID_ARG, AR_ERR_CUDA. */
+int ar_comm_export(const void* buffer, void* handle);
+
+/* Creates this rank's communicator: rank in [0, world), world in
+ * [1, AR_MAX_RANKS], buffer = this rank's registered buffer (16-byte
+ * aligned) of buffer_bytes >= ar_comm_buffer_size(world, max_bytes),
+ * handles = world * AR_IPC_HANDLE_BYTES bytes (host), rank q's at q (this
+ * rank's own is not read).  Maps every peer's buffer (cudaIpcOpenMemHandle)
+ * and zeroes this rank's flag words (synchronously).  On success *comm is
+ * the handle to pass to ar_allreduce_peer and ar_comm_destroy.
+ * Errors: AR_ERR_INVALID_ARG, AR_ERR_WORKSPACE (buffer too small),
+ *         AR_ERR_CUDA (a mapping or the zeroing failed; nothing is kept). */
+int ar_comm_create(int rank, int world, void* buffer, size_t buffer_bytes, size_t max_bytes, const void* handles,
+                   ar_comm** comm);
+
+/* Unmaps the peers' buffers and frees the communicator (the caller frees
+ * its own buffer).  Errors: AR_ERR_INVALID_ARG, AR_ERR_CUDA. */
+int ar_comm_destroy(ar_comm* comm);
+
+/*
+ * ar_allreduce_peer -- out = sum over the ranks of `input`, n elements of
+ * dtype, on every rank.  input and out: this rank's device memory, 16-byte
+ * aligned; out may equal input.  n * element size <= max_bytes.
+ *   strategy  AR_ONESHOT: every rank reads all n elements of every peer.
+ *             AR_TWOSHOT: rank r reduces slice r of every peer (the
+ *             reduce-scatter) and gathers the other slices from their
+ *             ranks (the all-gather).  AR_AUTO: one-shot for up to 2 ranks
+ *             or under 1 MiB, two-shot beyond (a size rule, not measured).
+ *             Values are bit-identical across strategies.
+ * Asynchronous on `stream`; stream-ordered with the calls before it.
+ * Errors: AR_ERR_INVALID_ARG, AR_ERR_UNSUPPORTED (dtype, strategy, or a
+ * misaligned pointer), AR_ERR_WORKSPACE (n beyond max_bytes), AR_ERR_CUDA.
+ */
+int ar_allreduce_peer(ar_comm* comm, const void* input, void* out, size_t n, int dtype, int strategy,
+                      ar_stream_t stream);
 
 #ifdef __cplusplus
 }

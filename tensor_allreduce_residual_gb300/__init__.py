@@ -36,6 +36,7 @@ AR_MAX_RANKS = 16
 # AllReduceStrategyConfig bit flags
 AR_CONFIG_USE_MEMCPY, AR_CONFIG_RESIDUAL_RMS_NORM = 1, 2
 AR_NOALLOC_SCRATCH_BYTES = 1 << 20
+AR_IPC_HANDLE_BYTES = 64
 
 STRATEGIES = {"NCCL": AR_NCCL, "ONESHOT": AR_ONESHOT, "TWOSHOT": AR_TWOSHOT, "AUTO": AR_AUTO}
 STRATEGY_NAMES = {v: k for k, v in STRATEGIES.items()}
@@ -132,6 +133,15 @@ def lib() -> ctypes.CDLL:
     L.ar_lamport_supported.restype = i
     L.ar_residual_rmsnorm_lamport.argtypes = [pvp, i, vp, vp, vp, ctypes.c_float, i, i, vp, vp, vp, sz, i, vp]
     L.ar_residual_rmsnorm_lamport.restype = i
+    L.ar_comm_buffer_size.argtypes, L.ar_comm_buffer_size.restype = [i, sz], sz
+    L.ar_comm_export.argtypes, L.ar_comm_export.restype = [vp, vp], i
+    L.ar_comm_create.argtypes = [i, i, vp, sz, sz, vp, ctypes.POINTER(vp)]
+    L.ar_comm_create.restype = i
+    L.ar_comm_destroy.argtypes, L.ar_comm_destroy.restype = [vp], i
+    L.ar_allreduce_peer.argtypes, L.ar_allreduce_peer.restype = [vp, vp, vp, sz, i, i, vp], i
+    if hasattr(L, "ar_comm_create_local"):   # the test build only
+        L.ar_comm_create_local.argtypes = [i, i, pvp, sz, sz, ctypes.POINTER(vp)]
+        L.ar_comm_create_local.restype = i
     _lib = L
     return L
 
@@ -492,3 +502,85 @@ def ar_residual_rmsnorm_lamport(partials: Sequence[torch.Tensor], residual: torc
         _stream_handle(stream))
     _check("ar_residual_rmsnorm_lamport", status)
     return out, residual_out
+
+
+# ------------------------------------------------------------ the all-reduce across GPUs (one process per GPU)
+
+def ar_comm_buffer_size(world: int, max_bytes: int) -> int:
+    """Bytes each rank registers for an all-reduce of up to max_bytes (0 for bad arguments)."""
+    return int(lib().ar_comm_buffer_size(world, max_bytes))
+
+
+def ar_comm_export(buffer: torch.Tensor) -> bytes:
+    """The CUDA IPC handle of a registered buffer, as AR_IPC_HANDLE_BYTES bytes."""
+    h = ctypes.create_string_buffer(AR_IPC_HANDLE_BYTES)
+    _check("ar_comm_export", lib().ar_comm_export(_dev_ptr(buffer, "buffer"), h))
+    return h.raw
+
+
+def gather_handles(handle: bytes, all_gather_object, world: int) -> bytes:
+    """Every rank's handle, in rank order, as one byte string of world * AR_IPC_HANDLE_BYTES bytes.
+
+    ``all_gather_object(out_list, obj)`` is the collective that fills out_list with every rank's obj
+    in rank order (torch.distributed.all_gather_object, or any equivalent)."""
+    if len(handle) != AR_IPC_HANDLE_BYTES:
+        raise ValueError("an IPC handle has AR_IPC_HANDLE_BYTES bytes")
+    got = [None] * world
+    all_gather_object(got, handle)
+    if any(not isinstance(h, (bytes, bytearray)) or len(h) != AR_IPC_HANDLE_BYTES for h in got):
+        raise ValueError("a rank sent no valid handle")
+    return b"".join(bytes(h) for h in got)
+
+
+class PeerComm:
+    """This rank's side of the all-reduce across the GPUs of one node (one process per GPU).
+
+    Registers a device buffer, exchanges its IPC handle with the other ranks
+    through ``all_gather_object`` and ``barrier`` (torch.distributed's by
+    default), and maps the peers' buffers (ar_comm_create).  allreduce(x)
+    then returns the sum over the ranks of every rank's x, on every rank.
+    """
+
+    def __init__(self, rank: int, world: int, max_bytes: int, device=None, all_gather_object=None, barrier=None):
+        self.rank, self.world, self.max_bytes = rank, world, max_bytes
+        nbytes = ar_comm_buffer_size(world, max_bytes)
+        if nbytes == 0:
+            raise ValueError("bad world size or max_bytes")
+        self.buffer = torch.empty(nbytes, dtype=torch.uint8, device=device if device is not None else "cuda")
+        handles = None
+        if world > 1:
+            if all_gather_object is None or barrier is None:
+                import torch.distributed as dist
+                all_gather_object = all_gather_object or dist.all_gather_object
+                barrier = barrier or dist.barrier
+            handles = gather_handles(ar_comm_export(self.buffer), all_gather_object, world)
+        comm = ctypes.c_void_p(0)
+        _check("ar_comm_create", lib().ar_comm_create(rank, world, _dev_ptr(self.buffer, "buffer"), nbytes,
+                                                      max_bytes, handles, ctypes.byref(comm)))
+        self._comm = comm
+        if world > 1:
+            barrier()   # every rank's flag words are zeroed before any rank signals into them
+
+    def allreduce(self, x: torch.Tensor, out: Optional[torch.Tensor] = None, strategy="AUTO",
+                  stream=None) -> torch.Tensor:
+        if self._comm is None:
+            raise RuntimeError("the communicator is closed")
+        if out is None:
+            out = torch.empty_like(x)
+        if out.numel() != x.numel() or out.dtype != x.dtype or not x.is_contiguous() or not out.is_contiguous():
+            raise ValueError("out must be a contiguous tensor of x's size and dtype")
+        _check("ar_allreduce_peer", lib().ar_allreduce_peer(self._comm, _dev_ptr(x, "x"), _dev_ptr(out, "out"),
+                                                            x.numel(), dtype_code(x.dtype), _strategy(strategy),
+                                                            _stream_handle(stream)))
+        return out
+
+    def close(self) -> None:
+        if self._comm is not None:
+            _check("ar_comm_destroy", lib().ar_comm_destroy(self._comm))
+            self._comm = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:   # pragma: no cover - interpreter teardown
+            pass

@@ -6,7 +6,9 @@ library next to this file.  Nothing is installed anywhere else.
 A second library, libar_test.so, is the same code with the test hooks
 compiled in (AR_TEST_HOOKS: the launch-shape override, the fault injection
 of the bounded-wait tests and the programmatic-launch switch, each read from
-the environment).  Only ar_api.cu differs, so only it is compiled twice.
+the environment, and a communicator over local buffers for the peer
+barrier's timeout test).  Only ar_api.cu and ar_peer.cu differ, so only
+they are compiled twice.
 The tests of forced launch shapes and of bounded waits, and the shape sweeps
 that build the AUTO table, load it; everything else loads libar.so, which
 reads no environment variable.
@@ -26,7 +28,8 @@ BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libar.so")
 TEST_LIB = os.path.join(PKG, "libar_test.so")
 
-SOURCES = ["ar_api.cu", "ar_kern_f32.cu", "ar_kern_f16.cu", "ar_kern_bf16.cu", "ar_noalloc.cu", "ar_host.cu"]
+SOURCES = ["ar_api.cu", "ar_kern_f32.cu", "ar_kern_f16.cu", "ar_kern_bf16.cu", "ar_noalloc.cu", "ar_host.cu",
+           "ar_peer.cu"]
 HEADERS = ["ar_internal.h", "ar_kernels.cuh", "ar_tma.cuh", "ar_lamport.cuh", "ar_launch.cuh", "ar_auto_table.h"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
@@ -59,6 +62,7 @@ def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) 
     objs = []
     units = [(src, os.path.join(BUILD, src.replace(".cu", ".o")), []) for src in SOURCES]
     units.append(("ar_api.cu", os.path.join(BUILD, "ar_api_test.o"), ["-DAR_TEST_HOOKS"]))
+    units.append(("ar_peer.cu", os.path.join(BUILD, "ar_peer_test.o"), ["-DAR_TEST_HOOKS"]))
     for src, obj, defs in units:
         cmd = [cc, *ARCH, *FLAGS, *defs, "-c", os.path.join(CSRC, src), "-o", obj]
         if ptxas_info:
@@ -77,7 +81,8 @@ def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) 
     if failed:
         raise RuntimeError(f"nvcc failed on {failed}")
     product = objs[:len(SOURCES)]
-    test = [o if not o.endswith(os.sep + "ar_api.o") else objs[-1] for o in product]
+    swap = {os.path.join(BUILD, "ar_api.o"): objs[-2], os.path.join(BUILD, "ar_peer.o"): objs[-1]}
+    test = [swap.get(o, o) for o in product]
     for lib, lib_objs in ((LIB, product), (TEST_LIB, test)):
         tmp = f"{lib}.{os.getpid()}.tmp"
         subprocess.run([cc, *ARCH, "-shared", "-o", tmp, *lib_objs], check=True)

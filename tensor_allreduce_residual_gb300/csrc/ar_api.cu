@@ -6,6 +6,7 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include <atomic>
 #include <cmath>
 #include <cstdint>
 #include <cstdio>
@@ -467,11 +468,24 @@ bool lamport_shape(int units_row, int tokens, int lanes, int R, OneShotShape* sh
     return false;
 }
 
-// Bytes of the Lamport buffer: the R slots, then the exchange area.
-size_t lamport_buffer_bytes(int R, int hidden, int tokens, int esize)
+// Bytes of the Lamport buffer for the launch shape `sh`: the blocks'
+// progress words, the R slots (a ring of at most kLamportRingGroups row
+// groups each), then the exchange area (per token).
+size_t lamport_buffer_bytes(int R, int hidden, int tokens, int esize, const OneShotShape& sh)
 {
-    return static_cast<size_t>(R) * tokens * hidden * esize +
+    const int csize = sh.mode == ar::kCluster ? sh.cluster : 1;
+    const int slot_rows = ar::lamport_slot_rows(tokens, sh.rows, csize);
+    return static_cast<size_t>(ar::kLamportProgressBytes) + static_cast<size_t>(R) * slot_rows * hidden * esize +
            static_cast<size_t>(tokens) * ar::kLamportRowWords * sizeof(uint32_t);
+}
+
+// A value of its own for every Lamport call, in [1, 2^31): the progress
+// words its blocks publish carry it, so words that earlier calls (or the
+// marker fill) left in the buffer never pass for this call's.
+uint32_t next_lamport_epoch()
+{
+    static std::atomic<uint32_t> counter{0};
+    return counter.fetch_add(1, std::memory_order_relaxed) % 0x7fffffffu + 1u;
 }
 
 }  // namespace
@@ -798,6 +812,11 @@ int ar_device_status(void)
             e = ed;
         total += n;
     }
+    unsigned int np = 0;
+    const cudaError_t ep = ar::take_peer_wait_timeouts(&np);
+    if (ep != cudaSuccess)
+        e = ep;
+    total += np;
     if (e != cudaSuccess)
         return AR_ERR_CUDA;
     return total != 0 ? AR_ERR_TIMEOUT : AR_OK;
@@ -898,7 +917,11 @@ size_t ar_lamport_buffer_size(int R, int hidden, int tokens, int dtype)
     const int esize = esize_of(dtype);
     if (R < 1 || R > AR_MAX_RANKS || hidden < 1 || tokens < 0 || esize == 0)
         return 0;
-    return round256(lamport_buffer_bytes(R, hidden, tokens, esize));
+    const int lanes = 16 / esize;
+    OneShotShape sh{};
+    if (hidden % lanes != 0 || !lamport_shape(hidden / lanes, tokens, lanes, R, &sh))
+        return 0;
+    return round256(lamport_buffer_bytes(R, hidden, tokens, esize, sh));
 }
 
 int ar_lamport_init(void* buffer, size_t bytes, int dtype, ar_stream_t stream)
@@ -963,7 +986,7 @@ int ar_residual_rmsnorm_lamport(const void* const* partials, int R, const void* 
     OneShotShape sh{};
     if (!lamport_shape(units_row, tokens, lanes, R, &sh))
         return AR_ERR_UNSUPPORTED;
-    const size_t need = lamport_buffer_bytes(R, hidden, tokens, esize);
+    const size_t need = lamport_buffer_bytes(R, hidden, tokens, esize, sh);
     if (lamport_buffer == nullptr || !aligned16(lamport_buffer) || lamport_bytes < need)
         return AR_ERR_WORKSPACE;
 
@@ -985,7 +1008,7 @@ int ar_residual_rmsnorm_lamport(const void* const* partials, int R, const void* 
     const int skip = test_lamport_skip_rank();
     const cudaError_t e = by_dtype(dtype, [&](auto tag) {
         using T = decltype(tag);
-        return ar::launch_fused_lamport<T>(a, lamport_buffer, sh, skip < R ? skip : -1, s);
+        return ar::launch_fused_lamport<T>(a, lamport_buffer, sh, skip < R ? skip : -1, next_lamport_epoch(), s);
     });
     if (e == cudaErrorInvalidConfiguration || e == cudaErrorCooperativeLaunchTooLarge ||
         e == cudaErrorNotSupported)

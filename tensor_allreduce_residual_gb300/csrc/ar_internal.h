@@ -180,19 +180,36 @@ cudaError_t launch_rmsnorm(const FusedArgs& a, bool packed, OneShotShape shape, 
 template <typename T>
 cudaError_t launch_rmsnorm_tma(const FusedArgs& a, OneShotShape shape, cudaStream_t s);
 
-// Lamport-style fused call.  Buffer: R slots of tokens * units_row 16-byte
-// vectors, then an exchange area of kLamportRowWords 32-bit words per row for
-// rows split over up to kLamportMaxSplit blocks.
+// Lamport-style fused call.  Buffer: one 64-bit progress word per block
+// (kLamportProgressBytes), then R slots of slot_rows * units_row 16-byte
+// vectors (a ring: row k of the call in ring row k mod ring_rows), then an
+// exchange area of kLamportRowWords 32-bit words per token for rows split
+// over up to kLamportMaxSplit blocks.
 constexpr int kLamportMaxSplit = 8;
 constexpr int kLamportRowWords = 16;
+
+// The ring is two steps of the launch's row groups deep; a slot holds at
+// most kLamportRingGroups groups, so the launch takes at most half that many
+// blocks.  Rows one rank's slot holds for `tokens` rows of `rows_per_group`
+// rows a group, or of rows split over `csize` > 1 blocks.
+constexpr int kLamportRingGroups = 1024;
+constexpr int kLamportProgressBytes = kLamportRingGroups / 2 * 8;
+inline int lamport_slot_rows(int tokens, int rows_per_group, int csize)
+{
+    const long long cap = csize > 1 ? kLamportRingGroups / csize : static_cast<long long>(kLamportRingGroups) * rows_per_group;
+    return tokens < cap ? tokens : static_cast<int>(cap);
+}
 
 // Pushes the R partials into the marker-filled buffer `lam`, then reduces
 // from it in the same cooperative launch.  shape.mode == kRegisters: tpr
 // threads a row; shape.mode == kCluster: each row split over shape.cluster
 // blocks of shape.tpr threads.  skip_rank >= 0 leaves that rank's pushes out
 // (tests).
+// `epoch`: this call's own value in [1, 2^31), which its blocks' progress
+// words carry.
 template <typename T>
-cudaError_t launch_fused_lamport(const FusedArgs& a, void* lam, OneShotShape shape, int skip_rank, cudaStream_t s);
+cudaError_t launch_fused_lamport(const FusedArgs& a, void* lam, OneShotShape shape, int skip_rank, uint32_t epoch,
+                                 cudaStream_t s);
 
 // Fills `bytes` of `buf` (16-byte aligned, bytes even) with T's empty marker.
 template <typename T>
@@ -202,5 +219,8 @@ cudaError_t launch_lamport_fill(void* buf, size_t bytes, cudaStream_t s);
 // the last call, which resets it.  Synchronous (reads device memory).
 template <typename T>
 cudaError_t take_wait_timeouts(unsigned int* count);
+
+// The same for the multi-GPU peer kernels (ar_peer.cu).
+cudaError_t take_peer_wait_timeouts(unsigned int* count);
 
 }  // namespace ar

@@ -14,25 +14,43 @@
 // again for the next call.  The data is its own ready flag.
 //
 // On one GPU the R ranks' writes are emulated inside the same launch.  The
-// buffer holds one slot per rank, slot r = [tokens][units_row] 16-byte
-// vectors at r * tokens * units_row.  Blocks push vectors of all R partials
-// into their slots (the peers' NVLink writes of the multi-GPU protocol) and
-// reduce rows as the register-resident one-shot kernel does -- tpr threads
-// per row, VPT vectors per thread, fp32 sums in rank order, bias, residual,
-// the row's sum of squares over a fixed tree -- reading each partial from
-// its slot instead of from the partial.  The rows a block reduces were
-// pushed by another block, so blocks wait on one another: the launch is
-// cooperative (all of its blocks resident at once, or the launch fails), so
-// every push it waits for is made by a block that is already running.
+// buffer holds one slot per rank (after the blocks' progress words); slot
+// r = [slot_rows][units_row] 16-byte vectors at r * slot_rows * units_row,
+// and row k of the call lives in ring
+// row k mod ring_rows of every slot (ring_rows <= slot_rows: two steps of the
+// grid's row groups, or all tokens when they are fewer).  Blocks push
+// vectors of all R partials into their slots (the peers' NVLink writes of
+// the multi-GPU protocol) and reduce rows as the register-resident one-shot
+// kernel does -- tpr threads per row, VPT vectors per thread, fp32 sums in
+// rank order, bias, residual, the row's sum of squares over a fixed tree --
+// reading each partial from its slot instead of from the partial.  The rows
+// a block reduces were pushed by another block, so blocks wait on one
+// another: the launch is cooperative (all of its blocks resident at once, or
+// the launch fails), so every push it waits for is made by a block that is
+// already running.
+//
+// Ring reuse.  A ring row is used again, by row k + ring_rows, once row k
+// has been reduced.  Each block publishes the last step it has finished
+// reducing (a release store after a block barrier); before pushing into a
+// ring row used earlier in the call, a block waits (acquire) until the block
+// that reduces that ring row has finished the step that last used it, so it
+// never overwrites an element not yet taken.  The reducer of row k +
+// ring_rows is the very thread that reduced row k (the schedule below keeps
+// slot position -> block fixed), so it cannot mistake row k's elements for
+// row k + ring_rows's: its own write of the marker comes first in program
+// order.  The ring is two steps deep, so a pusher waits only on a reduce two
+// steps back, and the whole ring (tens of MB at prefill size) stays in L2
+// instead of the buffer streaming through DRAM.
 //
 // Memory ordering.  Pushes are st.relaxed.gpu and polls ld.relaxed.gpu, both
 // of 16 bytes: each 2- or 4-byte element is written once, from the marker to
 // its value, and read until it is no longer the marker, so a vector read
 // part-way through a push shows some elements still empty and is read
 // again.  No fence is needed: nothing but the element itself is published.
-// The marker is written back with a plain store by the one thread that read
-// the element; the next call's pushes are ordered after it by the kernel
-// boundary.
+// The marker is written back with a relaxed store by the one thread that read
+// the element: a pusher that reuses the ring row observes it with a relaxed
+// poll, and per-element coherence orders the marker (and the read before it)
+// before the new push.  The next call's pushes follow the kernel boundary.
 //
 // Waits are bounded: a poll that has not seen its element after
 // kWaitLimitNs gives up, counts the event in g_wait_timeouts (read by the
@@ -145,7 +163,7 @@ __device__ __forceinline__ void lamport_take(uint4* lam, uint64_t slot_units, in
             v[r] = lamport_poll<T>(lam + r * slot_units + i, v[r], gave_up);
 #pragma unroll
         for (int r = 0; r < R_CT; ++r)
-            st16(lam + r * slot_units + i, lamport_empty<T>());
+            st_relaxed16(lam + r * slot_units + i, lamport_empty<T>());
         Lanes<T>::unpack(v[0], x);
 #pragma unroll
         for (int r = 1; r < R_CT; ++r) {
@@ -157,7 +175,7 @@ __device__ __forceinline__ void lamport_take(uint4* lam, uint64_t slot_units, in
         for (int r = 0; r < R; ++r) {
             uint4* p = lam + r * slot_units + i;
             const uint4 v = lamport_poll<T>(p, ld_relaxed16(p), gave_up);
-            st16(p, lamport_empty<T>());
+            st_relaxed16(p, lamport_empty<T>());
             float t[L];
             Lanes<T>::unpack(v, t);
             if (r == 0) {
@@ -241,28 +259,64 @@ __device__ __forceinline__ float lamport_exchange(uint32_t* xr, int c, int csize
     return tot;
 }
 
-// Pushes vector i of every partial into its rank's slot (skip_rank >= 0:
-// not that rank's).
+// Pushes vector i of every partial (at element index `src` of each partial)
+// into its rank's slot at ring index `dst` (skip_rank >= 0: not that
+// rank's).
 template <typename T, int R_CT>
-__device__ __forceinline__ void lamport_push(const FusedArgs& a, uint4* lam, uint64_t slot_units, int R, uint64_t i,
-                                             int skip_rank)
+__device__ __forceinline__ void lamport_push(const FusedArgs& a, uint4* lam, uint64_t slot_units, int R, uint64_t src,
+                                             uint64_t dst, int skip_rank)
 {
     if constexpr (R_CT > 0) {
         uint4 v[R_CT];
 #pragma unroll
         for (int r = 0; r < R_CT; ++r)
-            v[r] = ld_stream16(static_cast<const uint4*>(a.partials[r]) + i);
+            v[r] = ld_stream16(static_cast<const uint4*>(a.partials[r]) + src);
 #pragma unroll
         for (int r = 0; r < R_CT; ++r)
             if (r != skip_rank)
-                st_relaxed16(lam + r * slot_units + i, lamport_clean<T>(v[r]));
+                st_relaxed16(lam + r * slot_units + dst, lamport_clean<T>(v[r]));
     } else {
         for (int r = 0; r < R; ++r) {
-            const uint4 v = ld_stream16(static_cast<const uint4*>(a.partials[r]) + i);
+            const uint4 v = ld_stream16(static_cast<const uint4*>(a.partials[r]) + src);
             if (r != skip_rank)
-                st_relaxed16(lam + r * slot_units + i, lamport_clean<T>(v));
+                st_relaxed16(lam + r * slot_units + dst, lamport_clean<T>(v));
         }
     }
+}
+
+// Progress of the blocks through the steps of one call: word b holds (call
+// epoch << 32) | (the last step block b has finished reducing).  The host
+// gives every call its own epoch in [1, 2^31), so words left by earlier calls
+// (or by the marker fill, whose high word has its top bit set) never match.
+__device__ __forceinline__ void lamport_publish(unsigned long long* w, unsigned long long v)
+{
+    asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(w), "l"(v) : "memory");
+}
+
+__device__ __forceinline__ unsigned long long lamport_progress(const unsigned long long* w)
+{
+    unsigned long long v;
+    asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(w) : "memory");
+    return v;
+}
+
+// Waits (bounded) until word *w shows this call's epoch and a step >= `step`.
+__device__ __forceinline__ void lamport_wait_progress(const unsigned long long* w, uint32_t epoch, uint32_t step,
+                                                      bool& gave_up)
+{
+    auto done = [&](unsigned long long v) {
+        return static_cast<uint32_t>(v >> 32) == epoch && static_cast<uint32_t>(v) >= step;
+    };
+    if (gave_up || done(lamport_progress(w)))
+        return;
+    const unsigned long long t0 = global_ns();
+    do {
+        __nanosleep(64);
+        if (done(lamport_progress(w)))
+            return;
+    } while (global_ns() - t0 <= kWaitLimitNs);
+    gave_up = true;
+    atomicAdd(&g_wait_timeouts, 1u);
 }
 
 // The fused kernel.  Packed path only (16-byte vectors).
@@ -274,59 +328,99 @@ __device__ __forceinline__ void lamport_push(const FusedArgs& a, uint4* lam, uin
 // threads on it; the slices' sums of squares meet in the exchange area
 // through the same protocol as the data.
 //
-// Schedule.  The groups are dealt out in steps of gridDim.x: in a step, block
-// b pushes the vectors of group base + b (the very vectors its threads would
-// reduce), then reduces group base + (b + 1) % n, which its neighbour
-// pushes in the same step (n = the step's groups).  Pushes never wait, and a
-// reduce waits only for pushes (and split-row shares) of its own step, so
-// the waits cannot form a cycle; gridDim.x is a multiple of csize, so no
-// split row straddles two steps.  A step's pushed vectors are polled while
-// they are still in L2, and the marker written back over them lands on the
-// same dirty L2 lines: each buffer line reaches DRAM about once instead of
-// being written, read back and written again.  (Pushing one step ahead of
-// the reduce measured slower: with two steps of pushes and the partials'
-// stream in between, the pushed lines left L2 before they were polled.)
-// `skip_rank` >= 0 leaves that rank's pushes out (tests of the bounded waits
-// only; -1 = none).
+// Schedule.  The groups are dealt out in steps of G = gridDim.x: in a step,
+// block b pushes the vectors of the group at position b (the very vectors
+// its threads would reduce), then reduces the group at position (b + 1) mod
+// G, which its neighbour pushes in the same step; a position the (short)
+// last step does not reach is skipped.  So position p is always pushed by
+// block p and reduced by block p - 1 (mod G), in every step -- which keeps
+// each ring row's reducer the same thread (see "Ring reuse" above).  A
+// reduce waits only for pushes (and split-row shares) of its own step and a
+// push only for the reduce of its ring row two steps back, so the waits
+// cannot form a cycle; G is a multiple of csize, so no split row straddles
+// two steps.  A step's pushed vectors are polled while they are still in
+// L2.  (Pushing one step ahead of the reduce measured slower: with two
+// steps of pushes in flight beside the partials' stream, more of the ring's
+// lines left L2 before they were polled.)
+// `slot_rows` is the rows each rank's slot holds (the buffer layout, set by
+// the host); `skip_rank` >= 0 leaves that rank's pushes out (tests of the
+// bounded waits only; -1 = none).
 template <typename T, int R_CT, int VPT>
 __global__ void __launch_bounds__(lamport_max_threads(VPT * Lanes<T>::V))
-k_fused_lamport(const FusedArgs a, uint4* lam, const int tpr, const int csize, const int skip_rank)
+k_fused_lamport(const FusedArgs a, uint4* lam_buffer, const int tpr, const int csize, const int skip_rank,
+                const int slot_rows, const uint32_t epoch)
 {
     pdl_enter();
     using U = Unit<T, true>;
     constexpr int L = U::L;
     __shared__ float red[2][32];
     __shared__ float tot_s[2];
+    uint4* lam = lam_buffer;
     const int R = R_CT > 0 ? R_CT : a.R;
-    const uint64_t slot_units = static_cast<uint64_t>(a.tokens) * a.units_row;
+    const uint64_t slot_units = static_cast<uint64_t>(slot_rows) * a.units_row;
     const bool split = csize > 1;
     const int rows = split ? 1 : static_cast<int>(blockDim.x) / tpr;
     const int lane = split ? static_cast<int>(threadIdx.x) : static_cast<int>(threadIdx.x & (tpr - 1));
     const int row_in_block = split ? 0 : static_cast<int>(threadIdx.x) / tpr;
     const int slice = split ? (a.units_row + csize - 1) / csize : a.units_row;
     const int groups = split ? a.tokens * csize : (a.tokens + rows - 1) / rows;
+    const int G = static_cast<int>(gridDim.x);
+    // Two steps of groups, in rows (never more than the slot holds).
+    const long long ring_groups_rows = split ? 2LL * G / csize : 2LL * G * rows;
+    const int ring_rows = static_cast<int>(min(static_cast<long long>(min(a.tokens, slot_rows)), ring_groups_rows));
+    // The buffer: the blocks' progress words, then the R slots, then the
+    // exchange area.
+    unsigned long long* progress = reinterpret_cast<unsigned long long*>(lam);
+    lam += kLamportProgressBytes / sizeof(uint4);
     uint32_t* xarea = reinterpret_cast<uint32_t*>(lam + static_cast<uint64_t>(R) * slot_units);
     const int b = static_cast<int>(blockIdx.x);
+    const int q = (b + 1) % G;  // position this block reduces in every step
+    const int reducer_of_mine = (b + G - 1) % G;  // the block that reduces the position this block pushes
+    const uint32_t nsteps = static_cast<uint32_t>((groups + G - 1) / G);
     bool gave_up = false;
-    int parity = 0;
-    for (int base = 0; base < groups; base += gridDim.x, parity ^= 1) {
-        const int n = min(static_cast<int>(gridDim.x), groups - base);
-        if (b >= n)
-            break;  // block-uniform: only the last step can be short
-        // The pushed group (this block's) and the reduced one (its neighbour's).
+
+    // Push the group at this block's position of step s, if the step reaches
+    // it (block-uniform).  A ring row used before in this call (by step
+    // s - 2) is pushed only once its reducer, the block before this one, has
+    // published that step: it has taken the row and written the marker back.
+    auto push_step = [&](uint32_t s) {
+        const int base = static_cast<int>(s) * G;
+        if (b >= min(G, groups - base))
+            return;
         const int gp = base + b;
-        const int gr = base + (b + 1) % n;
         const int p_row = split ? gp / csize : gp * rows + row_in_block;
         const int p_begin = split ? (gp % csize) * slice : 0;
         const int p_end = min(p_begin + slice, a.units_row);
         const bool p_ok = p_row < a.tokens;
         const uint64_t p_off = static_cast<uint64_t>(p_row) * a.units_row;
+        const uint64_t p_ring = static_cast<uint64_t>(p_row % ring_rows) * a.units_row;
+        if ((split ? gp / csize : gp * rows) >= ring_rows) {
+            if (threadIdx.x == 0)
+                lamport_wait_progress(progress + reducer_of_mine, epoch, s - 2, gave_up);
+            __syncthreads();
+        }
+        // Vector by vector, all R ranks' loads in flight at once.
+#pragma unroll
+        for (int k = 0; k < VPT; ++k) {
+            const int j = p_begin + lane + k * tpr;
+            if (p_ok && j < p_end)
+                lamport_push<T, R_CT>(a, lam, slot_units, R, p_off + j, p_ring + j, skip_rank);
+        }
+    };
+
+    int parity = 0;
+    for (uint32_t step = 0; step < nsteps; ++step, parity ^= 1) {
+        const int base = static_cast<int>(step) * G;
+        const int n = min(G, groups - base);
+        const bool do_reduce = q < n;  // block-uniform
+        const int gr = base + q;
         const int row = split ? gr / csize : gr * rows + row_in_block;
         const int c = split ? gr % csize : 0;
         const int j_begin = c * slice;
         const int j_end = min(j_begin + slice, a.units_row);
-        const bool row_ok = row < a.tokens;
+        const bool row_ok = do_reduce && row < a.tokens;
         const uint64_t row_off = static_cast<uint64_t>(row) * a.units_row;
+        const uint64_t row_ring = static_cast<uint64_t>(row % ring_rows) * a.units_row;
 
         // The residual of the reduced group does not depend on the buffer:
         // its loads go out first and complete behind the push.
@@ -337,13 +431,12 @@ k_fused_lamport(const FusedArgs a, uint4* lam, const int tpr, const int csize, c
             if (row_ok && j < j_end)
                 rv[k] = U::load(a.residual, row_off + j);
         }
-
-        // Push: vector by vector, all R ranks' loads in flight at once.
-#pragma unroll
-        for (int k = 0; k < VPT; ++k) {
-            const int j = p_begin + lane + k * tpr;
-            if (p_ok && j < p_end)
-                lamport_push<T, R_CT>(a, lam, slot_units, R, p_off + j, skip_rank);
+        push_step(step);
+        if (!do_reduce) {
+            __syncthreads();
+            if (threadIdx.x == 0)
+                lamport_publish(progress + b, (static_cast<unsigned long long>(epoch) << 32) | step);
+            continue;
         }
 
         // Reduce: take every rank's vector from the buffer, then bias and
@@ -358,7 +451,7 @@ k_fused_lamport(const FusedArgs a, uint4* lam, const int tpr, const int csize, c
             for (int l = 0; l < L; ++l)
                 x[k][l] = 0.0f;
             if (row_ok && j < j_end)
-                lamport_take<T, R_CT>(lam, slot_units, R, row_off + j, x[k], gave_up);
+                lamport_take<T, R_CT>(lam, slot_units, R, row_ring + j, x[k], gave_up);
         }
 #pragma unroll
         for (int k = 0; k < VPT; ++k) {
@@ -404,6 +497,12 @@ k_fused_lamport(const FusedArgs a, uint4* lam, const int tpr, const int csize, c
                 U::store(a.out, row_off + j, y);
             }
         }
+        // Every thread of the block has taken its vectors of this step and
+        // written the marker back: publish the step (the release covers the
+        // whole block's stores through the barrier before it).
+        __syncthreads();
+        if (threadIdx.x == 0)
+            lamport_publish(progress + b, (static_cast<unsigned long long>(epoch) << 32) | step);
     }
 }
 

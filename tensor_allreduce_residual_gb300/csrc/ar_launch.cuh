@@ -305,10 +305,11 @@ cudaError_t launch_fused_twoshot(const FusedArgs& a, bool packed, cudaStream_t s
 // Lamport-style fused kernel: one cooperative launch (all blocks resident at
 // once, which its blocks' waits on one another need).  One block per row
 // group (rows, or row slices when rows are split), capped at the blocks that
-// fit on the device at once (rounded down to whole split rows); blocks take
-// the groups in steps of the grid.
+// fit on the device at once and at half the ring's groups (rounded down to
+// whole split rows); blocks take the groups in steps of the grid.
 template <typename T, int R_CT, int VPT>
-static cudaError_t run_lamport(const FusedArgs& a, void* lam, OneShotShape sh, int skip_rank, cudaStream_t s)
+static cudaError_t run_lamport(const FusedArgs& a, void* lam, OneShotShape sh, int skip_rank, uint32_t epoch,
+                               cudaStream_t s)
 {
     auto kernel = k_fused_lamport<T, R_CT, VPT>;
     const int threads = sh.tpr * sh.rows;
@@ -328,10 +329,14 @@ static cudaError_t run_lamport(const FusedArgs& a, void* lam, OneShotShape sh, i
     if (groups > INT_MAX || (csize > 1 && sh.rows != 1))
         return cudaErrorInvalidConfiguration;
     // Whole steps of split rows: the grid is a multiple of csize.
-    const long long cap = static_cast<long long>(sms) * per_sm / csize * csize;
+    long long cap = static_cast<long long>(sms) * per_sm;
+    if (cap > kLamportRingGroups / 2)
+        cap = kLamportRingGroups / 2;
+    cap = cap / csize * csize;
     if (cap < csize)
         return cudaErrorInvalidConfiguration;
     const long long grid = groups < cap ? groups : cap;
+    const int slot_rows = lamport_slot_rows(a.tokens, sh.rows, csize);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(grid));
     cfg.blockDim = dim3(threads);
@@ -342,30 +347,32 @@ static cudaError_t run_lamport(const FusedArgs& a, void* lam, OneShotShape sh, i
     attr[0].val.cooperative = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kernel, a, static_cast<uint4*>(lam), sh.tpr, csize, skip_rank);
+    return cudaLaunchKernelEx(&cfg, kernel, a, static_cast<uint4*>(lam), sh.tpr, csize, skip_rank, slot_rows, epoch);
 }
 
 template <typename T, int R_CT>
-static cudaError_t lamport_vpt(const FusedArgs& a, void* lam, OneShotShape sh, int skip_rank, cudaStream_t s)
+static cudaError_t lamport_vpt(const FusedArgs& a, void* lam, OneShotShape sh, int skip_rank, uint32_t epoch,
+                               cudaStream_t s)
 {
     switch (sh.vpt) {
-    case 1: return run_lamport<T, R_CT, 1>(a, lam, sh, skip_rank, s);
-    case 2: return run_lamport<T, R_CT, 2>(a, lam, sh, skip_rank, s);
-    case 4: return run_lamport<T, R_CT, 4>(a, lam, sh, skip_rank, s);
-    case 8: return run_lamport<T, R_CT, 8>(a, lam, sh, skip_rank, s);
+    case 1: return run_lamport<T, R_CT, 1>(a, lam, sh, skip_rank, epoch, s);
+    case 2: return run_lamport<T, R_CT, 2>(a, lam, sh, skip_rank, epoch, s);
+    case 4: return run_lamport<T, R_CT, 4>(a, lam, sh, skip_rank, epoch, s);
+    case 8: return run_lamport<T, R_CT, 8>(a, lam, sh, skip_rank, epoch, s);
     default: return cudaErrorInvalidValue;
     }
 }
 
 template <typename T>
-cudaError_t launch_fused_lamport(const FusedArgs& a, void* lam, OneShotShape sh, int skip_rank, cudaStream_t s)
+cudaError_t launch_fused_lamport(const FusedArgs& a, void* lam, OneShotShape sh, int skip_rank, uint32_t epoch,
+                                 cudaStream_t s)
 {
     switch (a.R) {
-    case 1: return lamport_vpt<T, 1>(a, lam, sh, skip_rank, s);
-    case 2: return lamport_vpt<T, 2>(a, lam, sh, skip_rank, s);
-    case 4: return lamport_vpt<T, 4>(a, lam, sh, skip_rank, s);
-    case 8: return lamport_vpt<T, 8>(a, lam, sh, skip_rank, s);
-    default: return lamport_vpt<T, 0>(a, lam, sh, skip_rank, s);
+    case 1: return lamport_vpt<T, 1>(a, lam, sh, skip_rank, epoch, s);
+    case 2: return lamport_vpt<T, 2>(a, lam, sh, skip_rank, epoch, s);
+    case 4: return lamport_vpt<T, 4>(a, lam, sh, skip_rank, epoch, s);
+    case 8: return lamport_vpt<T, 8>(a, lam, sh, skip_rank, epoch, s);
+    default: return lamport_vpt<T, 0>(a, lam, sh, skip_rank, epoch, s);
     }
 }
 
@@ -407,5 +414,5 @@ cudaError_t take_wait_timeouts(unsigned int* count)
     template cudaError_t ar::launch_rmsnorm<T>(const ar::FusedArgs&, bool, ar::OneShotShape, cudaStream_t);      \
     template cudaError_t ar::launch_rmsnorm_tma<T>(const ar::FusedArgs&, ar::OneShotShape, cudaStream_t);     \
     template cudaError_t ar::launch_fused_lamport<T>(const ar::FusedArgs&, void*, ar::OneShotShape, int,       \
-                                                     cudaStream_t);                                          \
+                                                     uint32_t, cudaStream_t);                                \
     template cudaError_t ar::launch_lamport_fill<T>(void*, size_t, cudaStream_t);

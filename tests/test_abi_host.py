@@ -40,7 +40,8 @@ def test_header_declares_the_expected_entry_points():
                  "ar_residual_rmsnorm", "ar_allreduce", "ar_query_strategy", "ar_query_launch", "ar_device_status",
                  "ar_rmsnorm", "ar_host_staging_size", "ar_residual_rmsnorm_host", "ar_config_workspace_size",
                  "ar_allreduce_config", "ar_lamport_buffer_size", "ar_lamport_init", "ar_lamport_supported",
-                 "ar_residual_rmsnorm_lamport"]:
+                 "ar_residual_rmsnorm_lamport", "ar_comm_buffer_size", "ar_comm_export", "ar_comm_create",
+                 "ar_comm_destroy", "ar_allreduce_peer"]:
         assert want in names, names
 
 
@@ -60,7 +61,8 @@ def test_test_library_exports_the_same_symbols(L):
         if nm.returncode != 0:
             pytest.skip("nm unavailable")
         exported[path] = set(re.findall(r"\bT (ar_\w+)", nm.stdout))
-    assert exported[ar.LIB_PATH] == exported[ar.TEST_LIB_PATH]
+    # the test build adds one test-only entry point, the communicator over local buffers
+    assert exported[ar.TEST_LIB_PATH] == exported[ar.LIB_PATH] | {"ar_comm_create_local"}
 
 
 _PLAN_PROBE = """
@@ -383,17 +385,23 @@ def test_lamport_argument_errors(L):
     assert _lamport(L, buf=None) == ar.AR_ERR_WORKSPACE
     assert _lamport(L, buf=(FAKE + 7 << 20) + 8) == ar.AR_ERR_WORKSPACE
     need = L.ar_lamport_buffer_size(2, 64, 4, ar.AR_FP32)
-    assert need == 2 * 4 * 64 * 4 + 4 * 64                 # the slots, then 64 bytes of exchange area a row
+    assert need == 2 * 4 * 64 * 4 + 4 * 64 + 4096   # the slots, 64 bytes of exchange area a row, progress words
     assert _lamport(L, buf_bytes=need - 1) == ar.AR_ERR_WORKSPACE
-    assert _lamport(L, buf_bytes=2 * 4 * 64 * 4) == ar.AR_ERR_WORKSPACE
+    assert _lamport(L, buf_bytes=2 * 4 * 64 * 4 + 4 * 64) == ar.AR_ERR_WORKSPACE
     # nothing to do
     assert _lamport(L, tokens=0, buf=None, residual=None, out=None) == ar.AR_OK
 
 
 def test_lamport_buffer_size_support_and_init(L):
-    assert L.ar_lamport_buffer_size(8, 8192, 1, ar.AR_BF16) == (8 * 8192 * 2 + 64 + 255) // 256 * 256
-    assert L.ar_lamport_buffer_size(3, 10, 1, ar.AR_FP16) == 256               # 60 + 64 bytes, rounded up
-    assert L.ar_lamport_buffer_size(8, 8192, 8192, ar.AR_BF16) == 8 * 8192 * 8192 * 2 + 8192 * 64
+    P = 512 * 8                                    # the progress words, one a block
+    assert L.ar_lamport_buffer_size(8, 8192, 1, ar.AR_BF16) == (8 * 8192 * 2 + 64 + P + 255) // 256 * 256
+    assert L.ar_lamport_buffer_size(3, 16, 1, ar.AR_FP16) == (96 + 64 + P + 255) // 256 * 256
+    assert L.ar_lamport_buffer_size(3, 10, 1, ar.AR_FP16) == 0                 # a shape the call cannot take
+    # the slots are a ring of at most 1024 row groups: 1024 rows of 8192 (one row a group) ...
+    assert L.ar_lamport_buffer_size(8, 8192, 8192, ar.AR_BF16) == 8 * 1024 * 8192 * 2 + 8192 * 64 + P
+    # ... or 8192 rows of 64 fp32 (16 vectors a row: 8 rows a group), then 64 bytes a token
+    assert L.ar_lamport_buffer_size(2, 64, 20000, ar.AR_FP32) == (2 * 8192 * 64 * 4 + 20000 * 64 + P + 255) // 256 * 256
+    assert L.ar_lamport_buffer_size(2, 64, 5000, ar.AR_FP32) == 2 * 5000 * 64 * 4 + 5000 * 64 + P
     for bad in [(0, 64, 1, ar.AR_FP32), (17, 64, 1, ar.AR_FP32), (2, 0, 1, ar.AR_FP32), (2, 64, -1, ar.AR_FP32),
                 (2, 64, 1, 9)]:
         assert L.ar_lamport_buffer_size(*bad) == 0
@@ -509,3 +517,44 @@ def test_binding_rejects_mismatched_tensors_before_any_call():
             call()
     with pytest.raises(ValueError):
         ar.ar_rmsnorm(res, torch.ones(H + 8, dtype=bf), 1e-6)
+
+
+def test_peer_comm_sizes_and_argument_errors(L):
+    """The multi-GPU communicator's calls reject bad arguments before any CUDA call."""
+    assert L.ar_comm_buffer_size(1, 1) == 16384 + 2 * 256                  # flag words, two data areas
+    assert L.ar_comm_buffer_size(8, 1 << 20) == 16384 + 2 * (1 << 20)
+    for bad in [(0, 1024), (17, 1024), (2, 0)]:
+        assert L.ar_comm_buffer_size(*bad) == 0
+    comm = ctypes.c_void_p(0)
+    size = L.ar_comm_buffer_size(2, 4096)
+    handles = ctypes.create_string_buffer(2 * ar.AR_IPC_HANDLE_BYTES)
+    for rank, world, buf, nbytes, maxb, h in [
+            (2, 2, FAKE, size, 4096, handles),          # rank out of range
+            (-1, 2, FAKE, size, 4096, handles),
+            (0, 17, FAKE, size, 4096, handles),         # world beyond AR_MAX_RANKS
+            (0, 2, None, size, 4096, handles),          # no buffer
+            (0, 2, FAKE + 8, size, 4096, handles),      # misaligned buffer
+            (0, 2, FAKE, size, 0, handles),             # nothing to reduce
+            (0, 2, FAKE, size, 4096, None)]:            # two ranks and no handles
+        assert L.ar_comm_create(rank, world, buf, nbytes, maxb, h, ctypes.byref(comm)) == ar.AR_ERR_INVALID_ARG
+    assert L.ar_comm_create(0, 2, FAKE, size - 1, 4096, handles, ctypes.byref(comm)) == ar.AR_ERR_WORKSPACE
+    assert L.ar_comm_create(0, 1, FAKE, size, 4096, None, None) == ar.AR_ERR_INVALID_ARG
+    assert L.ar_comm_destroy(None) == ar.AR_ERR_INVALID_ARG
+    assert L.ar_comm_export(None, handles) == ar.AR_ERR_INVALID_ARG
+    assert L.ar_allreduce_peer(None, FAKE, FAKE, 16, ar.AR_FP16, ar.AR_AUTO, None) == ar.AR_ERR_INVALID_ARG
+
+
+def test_gather_handles_orders_by_rank():
+    """The handle exchange concatenates every rank's handle in rank order and refuses short ones."""
+    hs = [bytes([r]) * ar.AR_IPC_HANDLE_BYTES for r in range(3)]
+
+    def fake_all_gather(out, obj):
+        out[:] = hs
+    assert ar.gather_handles(hs[1], fake_all_gather, 3) == b"".join(hs)
+    with pytest.raises(ValueError):
+        ar.gather_handles(b"short", fake_all_gather, 3)
+
+    def broken(out, obj):
+        out[:] = [hs[0], None, hs[2]]
+    with pytest.raises(ValueError):
+        ar.gather_handles(hs[0], broken, 3)

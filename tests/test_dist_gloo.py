@@ -8,6 +8,11 @@ returns the slowest rank's time on every rank, and that computing each
 rank's block on its own gives the same rows as computing the whole batch
 (rows are independent, so no collective is needed).  The per-row results
 come from the oracle, on the CPU.
+
+The all-reduce across GPUs (PeerComm) exchanges its ranks' IPC handles through
+torch.distributed before any device work: that exchange runs here on gloo
+(with stand-in handle bytes), and must give every rank all handles in rank
+order.
 """
 import os
 import socket
@@ -58,7 +63,11 @@ def _rank_main(rank: int, world: int, port: int, results):
         whole = oracle.residual_rmsnorm(glob.partials, glob.bias, glob.residual, glob.weight, glob.eps, "bf16")
         same = (torch.equal(mine[0].view(torch.int16), whole[0][b:e].view(torch.int16)) and
                 torch.equal(mine[1].view(torch.int16), whole[1][b:e].view(torch.int16)))
-        results[rank] = {"tiles": gathered, "slowest": slowest, "same": same}
+        # 4. The peer communicator's handle exchange, in rank order on every rank.
+        import tensor_allreduce_residual_gb300 as ar
+        handle = bytes([rank + 1]) * ar.AR_IPC_HANDLE_BYTES
+        table = ar.gather_handles(handle, dist.all_gather_object, world)
+        results[rank] = {"tiles": gathered, "slowest": slowest, "same": same, "handles": table}
         dist.barrier()
     finally:
         dist.destroy_process_group()
@@ -102,3 +111,8 @@ def test_max_over_ranks_is_the_slowest_rank(rank_results):
 
 def test_each_rank_block_alone_equals_the_whole_batch(rank_results):
     assert all(rank_results[r]["same"] for r in range(WORLD))
+
+
+def test_peer_handles_are_exchanged_in_rank_order(rank_results):
+    want = b"".join(bytes([r + 1]) * 64 for r in range(WORLD))
+    assert [rank_results[r]["handles"] for r in range(WORLD)] == [want] * WORLD

@@ -64,6 +64,14 @@ def all_marker(buf, dtype, nbytes):
     return bool(torch.all(v == m))
 
 
+PROGRESS = 4096   # the buffer starts with the blocks' progress words
+
+
+def slots_empty(buf, dtype):
+    """The slots and the exchange area (everything after the progress words) hold the marker."""
+    return all_marker(buf[PROGRESS:], dtype, buf.numel() - PROGRESS)
+
+
 def run(inp, buf=None, **kw):
     out, res = ar.ar_residual_rmsnorm_lamport([dev(p) for p in inp.partials], dev(inp.residual), dev(inp.weight),
                                               inp.eps, bias=dev(inp.bias), buffer=buf, **kw)
@@ -86,13 +94,15 @@ def _inputs(R, T, H, dtype, bias=True, seed=0):
     (16, 3, 2048, "bf16", True), (1, 9, 512, "fp16", False), (4, 33, 8200, "bf16", True),
     (2, 2, 16384, "bf16", True),       # the longest row class (8 vectors a thread)
     (5, 300, 768, "fp16", True),       # rows in groups of several per block, blocks striding
+    (4, 3000, 1024, "bf16", True),     # more rows than the ring holds: ring rows reused within the call
+    (2, 20000, 64, "fp32", True),      # the same with 8 rows a group
 ])
 def test_parity_with_oracle(R, T, H, dtype, bias):
     inp = _inputs(R, T, H, dtype, bias, seed=R * 100 + T)
     buf = ar.lamport_buffer(R, H, T, workloads.DTYPES[dtype])
     out, res = run(inp, buf)
     check(inp, out.cpu(), res.cpu(), f"R{R} T{T} H{H} {dtype}")
-    assert all_marker(buf, dtype, buf.numel())            # the slots and the exchange area
+    assert slots_empty(buf, dtype)
     assert ar.ar_device_status() == ar.AR_OK
 
 
@@ -104,12 +114,26 @@ def test_one_buffer_serves_a_sequence_of_calls():
         inp = _inputs(R, T, H, "bf16", bias=False, seed=seed)
         out, res = run(inp, buf)
         check(inp, out.cpu(), res.cpu(), f"call {seed}")
-        assert all_marker(buf, "bf16", buf.numel())
+        assert slots_empty(buf, "bf16")
     # a smaller call on the same (larger) buffer uses its front part only
     inp = _inputs(R, 3, H, "bf16", bias=False, seed=4)
     out, res = run(inp, buf)
     check(inp, out.cpu(), res.cpu(), "smaller call")
-    assert all_marker(buf, "bf16", buf.numel())
+    assert slots_empty(buf, "bf16")
+
+
+def test_ring_reuse_over_a_sequence_of_calls():
+    """Rows beyond the ring reuse its rows within a call (each push waits for its row to be empty
+    again); three such calls in a row on one buffer, all correct, the buffer left empty after each."""
+    R, T, H = 8, 2500, 2048
+    buf = ar.lamport_buffer(R, H, T, torch.bfloat16)
+    assert buf.numel() < R * T * H * 2          # the slots hold fewer rows than the call
+    for seed in (5, 6, 7):
+        inp = _inputs(R, T, H, "bf16", bias=seed != 6, seed=seed)
+        out, res = run(inp, buf)
+        check(inp, out.cpu(), res.cpu(), f"ring call {seed}")
+        assert slots_empty(buf, "bf16")
+    assert ar.ar_device_status() == ar.AR_OK
 
 
 @pytest.mark.parametrize("dtype", ["fp32", "fp16", "bf16"])
@@ -226,7 +250,7 @@ def test_full_size_prefill_sampled_rows():
                                 [p[ridx].contiguous() for p in inp.partials], inp.residual[ridx].contiguous(),
                                 inp.weight, inp.bias)
     check(sub, out[ridx.cuda()].cpu(), res[ridx.cuda()].cpu(), "prefill")
-    assert all_marker(buf, "bf16", buf.numel())
+    assert slots_empty(buf, "bf16")
     assert ar.ar_device_status() == ar.AR_OK
 
 
