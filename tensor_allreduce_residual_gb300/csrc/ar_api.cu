@@ -440,17 +440,39 @@ int lamport_split_rule(int tokens, int R, int units_row)
     return tokens <= 8 && static_cast<long long>(R) * units_row >= 8192 ? 4 : 1;
 }
 
+// Rows not split, at least this many: separate push and reduce warps
+// (k_fused_lamport_ws), when the reduce side has at most 256 threads of at
+// most 4 vectors each.
+// Measured at R=8 bf16 H=8192: 498-532 us against 569-570 us at 8192
+// rows, 136 against 148 us at 2048, 74-77 against 80 us at 1024, but 25
+// against 19 us at 256.
+constexpr int kLamportRolesMinTokens = 1024;
+
+// Ring depth of the Lamport buffer, in grid steps.  Deeper rings measured
+// slower (3: 565-594 us, 4: 631 us against 532-570 us at 8192 rows of R=8
+// bf16 H=8192): more of the ring leaves L2 before it is polled.
+constexpr int kLamportRingSteps = 2;
+
 bool lamport_shape(int units_row, int tokens, int lanes, int R, OneShotShape* sh)
 {
+    const ShapeOverride& ov = shape_override();
     auto fits = [&](int vpt) {
-        return oneshot_shape(units_row, vpt, lanes, true, ar::kRegisters, R, sh) &&
-               sh->tpr * sh->rows <= ar::lamport_max_threads(vpt * lanes);
+        if (!(oneshot_shape(units_row, vpt, lanes, true, ar::kRegisters, R, sh) &&
+              sh->tpr * sh->rows <= ar::lamport_max_threads(vpt * lanes)))
+            return false;
+        const bool roles_fit = sh->tpr * sh->rows <= 256 && vpt <= 4;
+        sh->roles = roles_fit && (ov.vpt > 0 ? ov.early : tokens >= kLamportRolesMinTokens) ? 1 : 0;
+        sh->stages = ov.vpt > 0 && ov.max_stages >= 2 && ov.max_stages <= ar::kLamportMaxRingSteps
+                         ? ov.max_stages
+                         : kLamportRingSteps;
+        return true;
     };
     auto fits_split = [&](int vpt, int c) {
+        sh->roles = 0;
+        sh->stages = kLamportRingSteps;
         return static_cast<long long>(tokens) * c <= INT32_MAX && cluster_shape(units_row, vpt, lanes, c, sh) &&
                sh->tpr <= ar::lamport_max_threads(vpt * lanes);
     };
-    const ShapeOverride& ov = shape_override();
     if (ov.vpt > 0 && ov.mode == ar::kRegisters && fits(ov.vpt))
         return true;
     if (ov.vpt > 0 && ov.mode == ar::kCluster && fits_split(ov.vpt, ov.blocks_per_sm))

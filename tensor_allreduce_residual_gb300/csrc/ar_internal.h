@@ -120,9 +120,10 @@ struct OneShotShape {
     int mode;
     int smem_bytes;
     int early_residual;  // write residual_out before the row barrier
-    int stages;          // kTma: ring slots per block
+    int stages;          // kTma: ring slots per block; Lamport call: ring depth in grid steps
     int blocks_per_sm;   // kTma: resident blocks per SM
     int cluster;         // kCluster: blocks per row (the cluster size); tpr is then threads per block
+    int roles;           // Lamport call: 1 = separate push and reduce warps (k_fused_lamport_ws)
 };
 
 // Largest block of the persistent one-shot kernel (it keeps the next row's
@@ -188,11 +189,13 @@ cudaError_t launch_rmsnorm_tma(const FusedArgs& a, OneShotShape shape, cudaStrea
 constexpr int kLamportMaxSplit = 8;
 constexpr int kLamportRowWords = 16;
 
-// The ring is two steps of the launch's row groups deep; a slot holds at
-// most kLamportRingGroups groups, so the launch takes at most half that many
-// blocks.  Rows one rank's slot holds for `tokens` rows of `rows_per_group`
+// The ring is ring_steps (2 .. kLamportMaxRingSteps, the launch shape's
+// `stages`) steps of the launch's row groups deep; a slot holds at most
+// kLamportRingGroups groups, so the launch takes at most that many over
+// ring_steps blocks.  Rows one rank's slot holds for `tokens` rows of `rows_per_group`
 // rows a group, or of rows split over `csize` > 1 blocks.
 constexpr int kLamportRingGroups = 1024;
+constexpr int kLamportMaxRingSteps = 4;
 constexpr int kLamportProgressBytes = kLamportRingGroups / 2 * 8;
 inline int lamport_slot_rows(int tokens, int rows_per_group, int csize)
 {

@@ -348,7 +348,7 @@ __device__ __forceinline__ void lamport_wait_progress(const unsigned long long* 
 template <typename T, int R_CT, int VPT>
 __global__ void __launch_bounds__(lamport_max_threads(VPT * Lanes<T>::V))
 k_fused_lamport(const FusedArgs a, uint4* lam_buffer, const int tpr, const int csize, const int skip_rank,
-                const int slot_rows, const uint32_t epoch)
+                const int slot_rows, const uint32_t epoch, const int ring_steps)
 {
     pdl_enter();
     using U = Unit<T, true>;
@@ -365,8 +365,9 @@ k_fused_lamport(const FusedArgs a, uint4* lam_buffer, const int tpr, const int c
     const int slice = split ? (a.units_row + csize - 1) / csize : a.units_row;
     const int groups = split ? a.tokens * csize : (a.tokens + rows - 1) / rows;
     const int G = static_cast<int>(gridDim.x);
-    // Two steps of groups, in rows (never more than the slot holds).
-    const long long ring_groups_rows = split ? 2LL * G / csize : 2LL * G * rows;
+    // ring_steps steps of groups, in rows (never more than the slot holds).
+    const long long ring_groups_rows =
+        split ? static_cast<long long>(ring_steps) * G / csize : static_cast<long long>(ring_steps) * G * rows;
     const int ring_rows = static_cast<int>(min(static_cast<long long>(min(a.tokens, slot_rows)), ring_groups_rows));
     // The buffer: the blocks' progress words, then the R slots, then the
     // exchange area.
@@ -381,8 +382,9 @@ k_fused_lamport(const FusedArgs a, uint4* lam_buffer, const int tpr, const int c
 
     // Push the group at this block's position of step s, if the step reaches
     // it (block-uniform).  A ring row used before in this call (by step
-    // s - 2) is pushed only once its reducer, the block before this one, has
-    // published that step: it has taken the row and written the marker back.
+    // s - ring_steps) is pushed only once its reducer, the block before this
+    // one, has published that step: it has taken the row and written the
+    // marker back.
     auto push_step = [&](uint32_t s) {
         const int base = static_cast<int>(s) * G;
         if (b >= min(G, groups - base))
@@ -396,7 +398,7 @@ k_fused_lamport(const FusedArgs a, uint4* lam_buffer, const int tpr, const int c
         const uint64_t p_ring = static_cast<uint64_t>(p_row % ring_rows) * a.units_row;
         if ((split ? gp / csize : gp * rows) >= ring_rows) {
             if (threadIdx.x == 0)
-                lamport_wait_progress(progress + reducer_of_mine, epoch, s - 2, gave_up);
+                lamport_wait_progress(progress + reducer_of_mine, epoch, s - ring_steps, gave_up);
             __syncthreads();
         }
         // Vector by vector, all R ranks' loads in flight at once.
@@ -502,6 +504,203 @@ k_fused_lamport(const FusedArgs a, uint4* lam_buffer, const int tpr, const int c
         // whole block's stores through the barrier before it).
         __syncthreads();
         if (threadIdx.x == 0)
+            lamport_publish(progress + b, (static_cast<unsigned long long>(epoch) << 32) | step);
+    }
+}
+
+// Barrier over `count` threads (a multiple of 32) of this block, by id: the
+// push and reduce warps of k_fused_lamport_ws synchronise apart.
+__device__ __forceinline__ void named_sync(int id, int count)
+{
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
+// row_sum over the `count` threads that reach named barrier `id` (threads
+// 0 .. count-1 of `t`'s numbering; the warps of one row are consecutive).
+__device__ __forceinline__ float row_sum_named(float v, int tpr, float* red, int id, int count, int t)
+{
+    if (tpr <= 32) {
+        for (int off = tpr >> 1; off > 0; off >>= 1)
+            v += __shfl_xor_sync(0xffffffffu, v, off);
+        return v;
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1)
+        v += __shfl_xor_sync(0xffffffffu, v, off);
+    const int warp = t >> 5;
+    if ((t & 31) == 0)
+        red[warp] = v;
+    named_sync(id, count);
+    const int wpr = tpr >> 5;
+    const int first = (warp / wpr) * wpr;
+    float s = red[first];
+    for (int w = 1; w < wpr; ++w)
+        s += red[first + w];
+    return s;
+}
+
+// The Lamport-style call with the push and the reduce in separate warps of
+// each block (rows not split; the reduce side has blockDim.x / 2 threads,
+// tpr a row, VPT vectors a thread, as k_fused_lamport).  Same buffer, ring,
+// schedule positions and progress words as k_fused_lamport: block b pushes
+// position b and reduces position (b + 1) mod G of every step.  But the push
+// warps run through the steps on their own, limited only by the ring (a
+// push into a reused ring row waits for its reducer's progress word), so a
+// reduce finds its neighbour's data already pushed, and the partials' loads
+// of later steps overlap the polls and the row reductions of earlier ones.
+// The push warps move two vectors of every rank per round (2 R loads in
+// flight a thread).  Barriers: id 1 among the reduce warps, id 2 among the
+// push warps; nothing after the split waits on the whole block.  Blocks of
+// at most 512 threads, VPT at most 4 (more would not fit 128 registers).
+template <typename T, int R_CT, int VPT>
+__global__ void __launch_bounds__(512, 1)
+k_fused_lamport_ws(const FusedArgs a, uint4* lam_buffer, const int tpr, const int skip_rank, const int slot_rows,
+                   const uint32_t epoch, const int ring_steps)
+{
+    pdl_enter();
+    using U = Unit<T, true>;
+    constexpr int L = U::L;
+    __shared__ float red[2][32];
+    uint4* lam = lam_buffer;
+    const int R = R_CT > 0 ? R_CT : a.R;
+    const int half = static_cast<int>(blockDim.x) / 2;
+    const bool pusher = static_cast<int>(threadIdx.x) >= half;
+    const int t = pusher ? static_cast<int>(threadIdx.x) - half : static_cast<int>(threadIdx.x);
+    const int rows = half / tpr;
+    const int lane = t & (tpr - 1);
+    const int row_in_block = t / tpr;
+    const int groups = (a.tokens + rows - 1) / rows;
+    const int G = static_cast<int>(gridDim.x);
+    const uint64_t slot_units = static_cast<uint64_t>(slot_rows) * a.units_row;
+    const int ring_rows =
+        static_cast<int>(min(static_cast<long long>(min(a.tokens, slot_rows)), static_cast<long long>(ring_steps) * G * rows));
+    unsigned long long* progress = reinterpret_cast<unsigned long long*>(lam);
+    lam += kLamportProgressBytes / sizeof(uint4);
+    const int b = static_cast<int>(blockIdx.x);
+    const uint32_t nsteps = static_cast<uint32_t>((groups + G - 1) / G);
+    bool gave_up = false;
+
+    if (pusher) {
+        const int reducer_of_mine = (b + G - 1) % G;
+        for (uint32_t step = 0; step < nsteps; ++step) {
+            const int base = static_cast<int>(step) * G;
+            if (b >= min(G, groups - base))
+                break;  // later steps are shorter still (push-uniform)
+            const int gp = base + b;
+            const int p_row = gp * rows + row_in_block;
+            const bool p_ok = p_row < a.tokens;
+            const uint64_t p_off = static_cast<uint64_t>(p_row) * a.units_row;
+            const uint64_t p_ring = static_cast<uint64_t>(p_row % ring_rows) * a.units_row;
+            if (gp * rows >= ring_rows) {  // a ring row used before in this call
+                if (t == 0)
+                    lamport_wait_progress(progress + reducer_of_mine, epoch, step - ring_steps, gave_up);
+                named_sync(2, half);
+            }
+            if constexpr (R_CT > 0) {
+#pragma unroll
+                for (int k = 0; k < VPT; k += 2) {
+                    uint4 v[2][R_CT];
+                    bool ok[2];
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const int j = lane + (k + h) * tpr;
+                        ok[h] = k + h < VPT && p_ok && j < a.units_row;
+                        if (ok[h]) {
+#pragma unroll
+                            for (int r = 0; r < R_CT; ++r)
+                                v[h][r] = ld_stream16(static_cast<const uint4*>(a.partials[r]) + p_off + j);
+                        }
+                    }
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const int j = lane + (k + h) * tpr;
+                        if (ok[h]) {
+#pragma unroll
+                            for (int r = 0; r < R_CT; ++r)
+                                if (r != skip_rank)
+                                    st_relaxed16(lam + r * slot_units + p_ring + j, lamport_clean<T>(v[h][r]));
+                        }
+                    }
+                }
+            } else {
+#pragma unroll
+                for (int k = 0; k < VPT; ++k) {
+                    const int j = lane + k * tpr;
+                    if (p_ok && j < a.units_row)
+                        lamport_push<T, R_CT>(a, lam, slot_units, R, p_off + j, p_ring + j, skip_rank);
+                }
+            }
+        }
+        return;
+    }
+
+    const int q = (b + 1) % G;  // the position this block reduces in every step
+    int parity = 0;
+    for (uint32_t step = 0; step < nsteps; ++step, parity ^= 1) {
+        const int base = static_cast<int>(step) * G;
+        const bool do_reduce = q < min(G, groups - base);  // reduce-uniform
+        const int gr = base + q;
+        const int row = gr * rows + row_in_block;
+        const bool row_ok = do_reduce && row < a.tokens;
+        const uint64_t row_off = static_cast<uint64_t>(row) * a.units_row;
+        const uint64_t row_ring = static_cast<uint64_t>(row % ring_rows) * a.units_row;
+        if (do_reduce) {
+            uint4 rv[VPT];
+#pragma unroll
+            for (int k = 0; k < VPT; ++k) {
+                const int j = lane + k * tpr;
+                if (row_ok && j < a.units_row)
+                    rv[k] = U::load(a.residual, row_off + j);
+            }
+            float x[VPT][L];
+            uint4 wv[VPT];
+            float ss = 0.0f;
+#pragma unroll
+            for (int k = 0; k < VPT; ++k) {
+                const int j = lane + k * tpr;
+#pragma unroll
+                for (int l = 0; l < L; ++l)
+                    x[k][l] = 0.0f;
+                if (row_ok && j < a.units_row)
+                    lamport_take<T, R_CT>(lam, slot_units, R, row_ring + j, x[k], gave_up);
+            }
+#pragma unroll
+            for (int k = 0; k < VPT; ++k) {
+                const int j = lane + k * tpr;
+                if (row_ok && j < a.units_row) {
+                    float tv[L];
+                    if (a.bias != nullptr) {
+                        U::to_float(U::load_cached(a.bias, j), tv);
+                        add_lanes<L>(x[k], tv);
+                    }
+                    U::to_float(rv[k], tv);
+                    add_lanes<L>(x[k], tv);
+                    wv[k] = U::load_cached(a.weight, j);
+                    U::store(a.residual_out, row_off + j, x[k]);
+#pragma unroll
+                    for (int l = 0; l < L; ++l)
+                        ss = fmaf(x[k][l], x[k][l], ss);
+                }
+            }
+            ss = row_sum_named(ss, tpr, red[parity], 1, half, t);
+            const float inv = inv_rms(ss, a.hidden, a.eps);
+#pragma unroll
+            for (int k = 0; k < VPT; ++k) {
+                const int j = lane + k * tpr;
+                if (row_ok && j < a.units_row) {
+                    float w[L], y[L];
+                    U::to_float(wv[k], w);
+#pragma unroll
+                    for (int l = 0; l < L; ++l)
+                        y[l] = x[k][l] * inv * w[l];
+                    U::store(a.out, row_off + j, y);
+                }
+            }
+        }
+        // Every reduce thread has taken its vectors of this step and written
+        // the marker back: publish the step.
+        named_sync(1, half);
+        if (t == 0)
             lamport_publish(progress + b, (static_cast<unsigned long long>(epoch) << 32) | step);
     }
 }

@@ -313,6 +313,9 @@ static cudaError_t run_lamport(const FusedArgs& a, void* lam, OneShotShape sh, i
 {
     auto kernel = k_fused_lamport<T, R_CT, VPT>;
     const int threads = sh.tpr * sh.rows;
+    const int ring_steps = sh.stages;
+    if (ring_steps < 2 || ring_steps > kLamportMaxRingSteps)
+        return cudaErrorInvalidValue;
     int dev = 0, sms = 0, per_sm = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e == cudaSuccess)
@@ -330,8 +333,8 @@ static cudaError_t run_lamport(const FusedArgs& a, void* lam, OneShotShape sh, i
         return cudaErrorInvalidConfiguration;
     // Whole steps of split rows: the grid is a multiple of csize.
     long long cap = static_cast<long long>(sms) * per_sm;
-    if (cap > kLamportRingGroups / 2)
-        cap = kLamportRingGroups / 2;
+    if (cap > kLamportRingGroups / ring_steps)
+        cap = kLamportRingGroups / ring_steps;
     cap = cap / csize * csize;
     if (cap < csize)
         return cudaErrorInvalidConfiguration;
@@ -347,13 +350,67 @@ static cudaError_t run_lamport(const FusedArgs& a, void* lam, OneShotShape sh, i
     attr[0].val.cooperative = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kernel, a, static_cast<uint4*>(lam), sh.tpr, csize, skip_rank, slot_rows, epoch);
+    return cudaLaunchKernelEx(&cfg, kernel, a, static_cast<uint4*>(lam), sh.tpr, csize, skip_rank, slot_rows, epoch,
+                              ring_steps);
+}
+
+// The same with separate push and reduce warps: blocks of 2 x tpr x rows
+// threads, rows never split.
+template <typename T, int R_CT, int VPT>
+static cudaError_t run_lamport_ws(const FusedArgs& a, void* lam, OneShotShape sh, int skip_rank, uint32_t epoch,
+                                  cudaStream_t s)
+{
+    auto kernel = k_fused_lamport_ws<T, R_CT, VPT>;
+    const int threads = 2 * sh.tpr * sh.rows;
+    const int ring_steps = sh.stages;
+    if (ring_steps < 2 || ring_steps > kLamportMaxRingSteps)
+        return cudaErrorInvalidValue;
+    if (sh.mode == kCluster || threads > 512)
+        return cudaErrorInvalidConfiguration;
+    int dev = 0, sms = 0, per_sm = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess)
+        e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e == cudaSuccess)
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads, 0);
+    if (e != cudaSuccess)
+        return e;
+    if (per_sm < 1)
+        return cudaErrorInvalidConfiguration;
+    const long long groups = (static_cast<long long>(a.tokens) + sh.rows - 1) / sh.rows;
+    if (groups > INT_MAX)
+        return cudaErrorInvalidConfiguration;
+    long long cap = static_cast<long long>(sms) * per_sm;
+    if (cap > kLamportRingGroups / ring_steps)
+        cap = kLamportRingGroups / ring_steps;
+    const long long grid = groups < cap ? groups : cap;
+    const int slot_rows = lamport_slot_rows(a.tokens, sh.rows, 1);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid));
+    cfg.blockDim = dim3(threads);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, a, static_cast<uint4*>(lam), sh.tpr, skip_rank, slot_rows, epoch,
+                              ring_steps);
 }
 
 template <typename T, int R_CT>
 static cudaError_t lamport_vpt(const FusedArgs& a, void* lam, OneShotShape sh, int skip_rank, uint32_t epoch,
                                cudaStream_t s)
 {
+    if (sh.roles) {
+        switch (sh.vpt) {
+        case 1: return run_lamport_ws<T, R_CT, 1>(a, lam, sh, skip_rank, epoch, s);
+        case 2: return run_lamport_ws<T, R_CT, 2>(a, lam, sh, skip_rank, epoch, s);
+        case 4: return run_lamport_ws<T, R_CT, 4>(a, lam, sh, skip_rank, epoch, s);
+        default: return cudaErrorInvalidValue;
+        }
+    }
     switch (sh.vpt) {
     case 1: return run_lamport<T, R_CT, 1>(a, lam, sh, skip_rank, epoch, s);
     case 2: return run_lamport<T, R_CT, 2>(a, lam, sh, skip_rank, epoch, s);

@@ -52,6 +52,9 @@ def main():
     # many more row groups than resident blocks: blocks stride over them
     big = fused(8, 2000, 1024, "bf16", 5)
     check(big, rows=[0, 1, 151, 152, 999, 1000, 1500, 1998, 1999])
+    # more rows than the ring holds, so ring rows are reused within the call
+    ring = fused(8, 3000, 2048, "bf16", 6)
+    check(ring, rows=[0, 1, 511, 512, 1023, 1024, 1025, 2047, 2048, 2999])
     # one buffer, several calls
     buf = ar.lamport_buffer(8, 8192, 8, torch.bfloat16)
     for seed in (11, 12):

@@ -52,7 +52,21 @@ def main():
     torch.cuda.synchronize()
     _check(g, out, res, "Lamport after timeout")
     assert ar.ar_device_status() == ar.AR_OK
-    print(f"lamport timeout ok ({took:.2f} s)")
+    # The same with separate push and reduce warps (many rows, the ring reused within the call):
+    # rank 1's pushes are left out, every poll of its slot runs out, the call returns.
+    h = workloads.fused_inputs(2, 3000, 1024, "bf16", partial_dist=("N", 0.0, 0.5),
+                               residual_dist=("N", 0.0, 4.0), bias_dist=None, weight_dist=("N", 1.0, 0.05),
+                               eps=1e-6, seed=3)
+    assert ar.ar_lamport_supported(2, 1024, 3000, torch.bfloat16) is not None
+    big = ar.lamport_buffer(2, 1024, 3000, torch.bfloat16)
+    t0 = time.time()
+    ar.ar_residual_rmsnorm_lamport([p.cuda() for p in h.partials], h.residual.cuda(), h.weight.cuda(), h.eps,
+                                   buffer=big)
+    torch.cuda.synchronize()
+    took2 = time.time() - t0
+    assert ar.ar_device_status() == ar.AR_ERR_TIMEOUT
+    assert 0.5 < took2 < 60.0, took2
+    print(f"lamport timeout ok ({took:.2f} s, {took2:.2f} s with separate push and reduce warps)")
 
 
 if __name__ == "__main__":

@@ -254,9 +254,11 @@ def test_full_size_prefill_sampled_rows():
     assert ar.ar_device_status() == ar.AR_OK
 
 
-@pytest.mark.parametrize("shape", ["1:0", "2:0", "4:0", "8:0", "1:4:0:2", "1:4:0:4", "1:4:0:8", "2:4:0:8"])
+@pytest.mark.parametrize("shape", ["1:0", "2:0", "4:0", "8:0", "1:4:0:2", "1:4:0:4", "1:4:0:8", "2:4:0:8",
+                                   "1:0:1", "2:0:1", "4:0:1"])
 def test_lamport_shape_parity(shape):
-    """Every launch shape the call can take, forced through the shape override in a child process."""
+    """Every launch shape the call can take, forced through the shape override in a child process
+    (third field 1: separate push and reduce warps, where the row fits them)."""
     env = dict(os.environ, AR_ONESHOT_SHAPE=shape)
     res = subprocess.run([sys.executable, "-m", "tests.lamport_shape_child"], cwd=ROOT, env=env,
                          capture_output=True, text=True, timeout=600)

@@ -3,9 +3,11 @@
 The kernel deals its groups (rows, or row slices when a row is split over
 C blocks) out in steps of the grid G: in a step, block b pushes the group at
 position b and then reduces the group at position (b + 1) mod G; a position
-that a short last step does not reach is skipped.  A split row's blocks
+that a short last step does not reach is skipped.  With separate push and
+reduce warps (rows not split), a block's pushes run through the steps on
+their own and its reduces on their own: two chains of program order.  A split row's blocks
 exchange their shares of the sum of squares and wait for all C of them.  The
-buffer is a ring two steps deep: group g lives in ring slot g mod 2G, and a
+buffer is a ring of D steps (2 by default): group g lives in ring slot g mod DG, and a
 block pushing a group into a slot that held an earlier group of the call
 first waits for the block that reduced that earlier group to publish the
 step in which it did so.  Blocks wait on one another, so the schedule must
@@ -50,7 +52,7 @@ def schedule_short_step_wraps(groups, G):
     return out
 
 
-def check(tokens, csize, rows, G, launcher_grid=True):
+def check(tokens, csize, rows, G, launcher_grid=True, roles=False, ring_steps=2):
     groups = tokens * csize if csize > 1 else -(-tokens // rows)
     sched = schedule(groups, G)
     pushed = [g for _, _, g, _ in sched if g is not None]
@@ -63,7 +65,7 @@ def check(tokens, csize, rows, G, launcher_grid=True):
         for row in range(tokens):
             assert len({step_of[row * csize + c] for c in range(csize)}) == 1
 
-    ring = 2 * G                                          # ring slots, in groups
+    ring = ring_steps * G                                 # ring slots, in groups
     pusher = {g: (s, b) for s, b, g, _ in sched if g is not None}
     reducer = {g: (s, b) for s, b, _, g in sched if g is not None}
     for g in range(ring, groups):                         # (4) one reducer block per ring slot
@@ -82,13 +84,20 @@ def check(tokens, csize, rows, G, launcher_grid=True):
             ps, pb = pusher[gr]
             edges[("push", ps, pb)].add(("share", s, b))        # the reduce polls the pushed group
         if gp is not None and gp >= ring:                       # (5) a reused slot: the progress wait
-            ws, wb = s - 2, (b + G - 1) % G                     # what the kernel waits for ...
+            ws, wb = s - ring_steps, (b + G - 1) % G            # what the kernel waits for ...
             assert reducer[gp - ring] == (ws, wb)               # ... is the reduce of the slot's last group
             edges[("done", ws, wb)].add(("push", s, b))
     steps = max(s for s, _, _, _ in sched) + 1
     for b in range(G):                                          # program order across steps
         for s0 in range(steps - 1):
-            edges[("done", s0, b)].add(("push", s0 + 1, b))
+            if roles:   # separate push and reduce warps: two chains per block
+                edges[("push", s0, b)].add(("push", s0 + 1, b))
+                edges[("done", s0, b)].add(("share", s0 + 1, b))
+            else:
+                edges[("done", s0, b)].add(("push", s0 + 1, b))
+        if roles:       # within a step the reduce no longer follows the block's own push
+            for s0 in range(steps):
+                edges[("push", s0, b)].discard(("share", s0, b))
     if csize > 1:                                               # a split row's exchange waits for every share
         for row in range(tokens):
             members = [reducer[row * csize + c] for c in range(csize)]
@@ -161,3 +170,26 @@ def test_a_short_last_step_must_not_change_a_ring_slot_reducer():
 def test_prefill_sized_rings(tokens, G):
     """Shapes of the GPU tests whose rows outnumber the ring: every slot reused several times."""
     check(tokens, 1, 1, G)
+
+
+def test_separate_push_and_reduce_warps_cover_every_group_without_cycles():
+    """The same rules when a block's push warps and reduce warps run apart (rows not split): pushes
+    ahead of their own block's reduces, limited only by the ring's progress waits."""
+    rng = random.Random(99)
+    for _ in range(200):
+        tokens = rng.choice([1, 2, 7, 33, 257, 1000, rng.randint(1, 5000)])
+        rows = rng.choice([1, 2, 4])
+        groups = -(-tokens // rows)
+        G = min(groups, rng.choice([1, 2, 5, 152, 304, 512, rng.randint(1, 512)]))
+        check(tokens, 1, rows, G, roles=True)
+
+
+@pytest.mark.parametrize("ring_steps", [3, 4])
+def test_deeper_rings(ring_steps):
+    rng = random.Random(ring_steps)
+    for _ in range(100):
+        tokens = rng.choice([1, 33, 700, 3000, rng.randint(1, 6000)])
+        rows = rng.choice([1, 2, 4])
+        groups = -(-tokens // rows)
+        G = min(groups, 1024 // ring_steps, rng.choice([1, 5, 152, 256, rng.randint(1, 341)]))
+        check(tokens, 1, rows, G, roles=rng.random() < 0.5, ring_steps=ring_steps)
