@@ -7,7 +7,10 @@
 // is AR_ONESHOT (1) or AR_TWOSHOT (2); `vpt` is the packed vectors each
 // thread of the one-shot kernel keeps per row (threads per row =
 // units_row / vpt rounded up to a power of two).  Shapes with no entry fall
-// back to the rule in ar_api.cu.
+// back to the rule in ar_api.cu.  The times in the comments are device time
+// per call: replayed graphs below 64 MB of algorithmic bytes per call, and
+// from 64 MB ("cold") back-to-back calls over input sets that together exceed
+// L2 several times, so that every call reads its inputs from DRAM.
 #pragma once
 
 namespace ar {
@@ -26,49 +29,48 @@ struct AutoEntry {
 };
 
 static const AutoEntry kAutoTable[] = {
-    {2, 2, 512, 1, 1, 1, 0, 1, 1, 0},  // tp_decode_R2_fp16_H4096 T=1: one-shot 2.493 us
-    {2, 2, 512, 2, 1, 1, 0, 1, 1, 0},  // tp_decode_R2_fp16_H4096 T=2: one-shot 2.419 us
-    {2, 2, 512, 4, 1, 1, 0, 1, 1, 0},  // tp_decode_R2_fp16_H4096 T=4: one-shot 2.429 us
-    {2, 2, 512, 8, 1, 1, 0, 1, 1, 0},  // tp_decode_R2_fp16_H4096 T=8: one-shot 2.445 us
-    {2, 2, 512, 16, 1, 1, 0, 1, 1, 0},  // tp_decode_R2_fp16_H4096 T=16: one-shot 2.445 us
-    {2, 2, 512, 32, 1, 2, 0, 1, 1, 0},  // tp_decode_R2_fp16_H4096 T=32: one-shot 2.557 us
-    {2, 2, 512, 64, 1, 1, 0, 1, 1, 0},  // tp_decode_R2_fp16_H4096 T=64: one-shot 2.554 us
-    {2, 2, 512, 256, 1, 2, 0, 1, 1, 0},  // tp_decode_R2_fp16_H4096 T=256: one-shot 3.094 us
-    {2, 2, 512, 1024, 1, 2, 0, 1, 1, 0},  // tp_decode_R2_fp16_H4096 T=1024: one-shot 6.112 us
-    {2, 2, 512, 2147483647, 1, 1, 0, 1, 1, 0},  // tp_decode_R2_fp16_H4096 T=8192: one-shot 52.349 us
-    {2, 2, 2048, 1, 1, 2, 4, 0, 8, 0},  // R2_bf16_H16384 T=1: one-shot 3.187 us
-    {2, 2, 2048, 64, 1, 2, 4, 1, 4, 0},  // R2_bf16_H16384 T=64: one-shot 4.422 us
-    {2, 2, 2048, 1024, 2, 0, 0, 0, 1, 0},  // R2_bf16_H16384 T=1024: two-shot 29.686 us
-    {2, 2, 2048, 2147483647, 2, 0, 0, 0, 1, 0},  // R2_bf16_H16384 T=4096: two-shot 120.256 us
-    {2, 3, 512, 1, 1, 1, 0, 1, 1, 0},  // R3_fp16_H4096 T=1: one-shot 2.902 us
-    {2, 3, 512, 64, 1, 1, 3, 1, 1, 2},  // R3_fp16_H4096 T=64: one-shot 2.979 us
-    {2, 3, 512, 2048, 1, 1, 0, 1, 1, 0},  // R3_fp16_H4096 T=2048: one-shot 17.574 us
-    {2, 3, 512, 2147483647, 1, 1, 3, 1, 1, 4},  // R3_fp16_H4096 T=8192: one-shot 62.422 us
-    {2, 4, 1024, 1, 1, 1, 4, 0, 8, 0},  // R4_fp16_H8192 T=1: one-shot 3.123 us
-    {2, 4, 1024, 64, 1, 2, 0, 1, 1, 0},  // R4_fp16_H8192 T=64: one-shot 3.414 us
-    {2, 4, 1024, 512, 1, 2, 0, 1, 1, 0},  // R4_fp16_H8192 T=65..512: the register shape that ran for T=1024's pick
-    {2, 4, 1024, 1024, 1, 4, 0, 1, 1, 0},  // R4_fp16_H8192 T=1024: one-shot 18.016 us (register shape)
-    {2, 4, 1024, 4096, 1, 4, 3, 1, 1, 4},  // R4_fp16_H8192 T=4096: one-shot 70.666 us
-    {2, 4, 1024, 2147483647, 1, 4, 3, 1, 1, 4},  // R4_fp16_H8192 T=8192: one-shot 137.034 us
-    {2, 8, 512, 1, 1, 1, 4, 0, 8, 0},  // R8_bf16_H4096 T=1: one-shot 2.966 us
-    {2, 8, 512, 64, 1, 1, 0, 1, 1, 0},  // R8_bf16_H4096 T=64: one-shot 3.085 us
-    {2, 8, 512, 1024, 1, 1, 3, 1, 1, 8},  // R8_bf16_H4096 T=1024: one-shot 12.307 us
-    {2, 8, 512, 4096, 1, 1, 3, 1, 1, 2},  // R8_bf16_H4096 T=4096: one-shot 55.19 us
-    {2, 8, 512, 2147483647, 1, 1, 3, 1, 1, 2},  // R8_bf16_H4096 T=8192: one-shot 106.445 us
-    {2, 8, 1024, 1, 1, 1, 4, 0, 8, 0},  // R8_bf16_H8192 T=1: one-shot 3.107 us
-    {2, 8, 1024, 8, 1, 1, 4, 1, 8, 0},  // R8_bf16_H8192 T=8: one-shot 3.325 us
-    {2, 8, 1024, 32, 1, 1, 4, 1, 8, 0},  // R8_bf16_H8192 T=32: one-shot 3.779 us
-    {2, 8, 1024, 64, 1, 2, 0, 1, 1, 0},  // R8_bf16_H8192 T=64: one-shot 3.968 us
-    {2, 8, 1024, 256, 1, 2, 0, 1, 1, 0},  // R8_bf16_H8192 T=256: one-shot 5.68 us
-    {2, 8, 1024, 512, 1, 2, 3, 1, 1, 0},  // R8_bf16_H8192 T=512: one-shot 12.717 us
-    {2, 8, 1024, 1024, 1, 4, 1, 0, 1, 0},  // R8_bf16_H8192 T=1024: one-shot 29.632 us
-    {2, 8, 1024, 2048, 1, 4, 3, 1, 1, 4},  // R8_bf16_H8192 T=2048: one-shot 55.331 us
-    {2, 8, 1024, 4096, 1, 2, 3, 1, 1, 2},  // R8_bf16_H8192 T=4096: one-shot 106.141 us
-    {2, 8, 1024, 2147483647, 1, 2, 3, 1, 1, 2},  // R8_bf16_H8192 T=8192: one-shot 207.29 us
-    {2, 16, 1024, 1, 1, 1, 4, 1, 8, 0},  // R16_bf16_H8192 T=1: one-shot 4.848 us
-    {2, 16, 1024, 64, 1, 1, 4, 1, 4, 0},  // R16_bf16_H8192 T=64: one-shot 5.734 us
-    {2, 16, 1024, 2048, 1, 4, 3, 1, 1, 2},  // R16_bf16_H8192 T=2048: one-shot 95.837 us
-    {2, 16, 1024, 2147483647, 1, 4, 3, 1, 1, 2},  // R16_bf16_H8192 T=8192: one-shot 363.971 us
+    {2, 2, 512, 1, 1, 1, 0, 1, 1, 0},  // tp_decode_R2_fp16_H4096 T=1: one-shot 2.47 us
+    {2, 2, 512, 2, 1, 1, 0, 0, 1, 0},  // tp_decode_R2_fp16_H4096 T=2: one-shot 2.352 us
+    {2, 2, 512, 4, 1, 1, 0, 1, 1, 0},  // tp_decode_R2_fp16_H4096 T=4: one-shot 2.349 us
+    {2, 2, 512, 8, 1, 1, 0, 1, 1, 0},  // tp_decode_R2_fp16_H4096 T=8: one-shot 2.406 us
+    {2, 2, 512, 16, 1, 1, 0, 1, 1, 0},  // tp_decode_R2_fp16_H4096 T=16: one-shot 2.381 us
+    {2, 2, 512, 32, 1, 1, 0, 1, 1, 0},  // tp_decode_R2_fp16_H4096 T=32: one-shot 2.39 us
+    {2, 2, 512, 64, 1, 1, 0, 1, 1, 0},  // tp_decode_R2_fp16_H4096 T=64: one-shot 2.48 us
+    {2, 2, 512, 256, 1, 2, 0, 1, 1, 0},  // tp_decode_R2_fp16_H4096 T=256: one-shot 3.005 us
+    {2, 2, 512, 1024, 1, 2, 0, 1, 1, 0},  // tp_decode_R2_fp16_H4096 T=1024: one-shot 6.128 us
+    {2, 2, 512, 2147483647, 1, 1, 0, 1, 1, 0},  // tp_decode_R2_fp16_H4096 T=8192: one-shot 52.01 us cold
+    {2, 2, 2048, 1, 1, 2, 4, 1, 8, 0},  // R2_bf16_H16384 T=1: one-shot 3.171 us
+    {2, 2, 2048, 64, 1, 2, 4, 1, 4, 0},  // R2_bf16_H16384 T=64: one-shot 4.403 us
+    {2, 2, 2048, 1024, 2, 0, 0, 0, 1, 0},  // R2_bf16_H16384 T=1024: two-shot 32.56 us cold
+    {2, 2, 2048, 2147483647, 1, 4, 2, 1, 1, 0},  // R2_bf16_H16384 T=4096: one-shot 112.376 us cold
+    {2, 3, 512, 1, 1, 1, 0, 1, 1, 0},  // R3_fp16_H4096 T=1: one-shot 2.918 us
+    {2, 3, 512, 64, 1, 1, 0, 1, 1, 0},  // R3_fp16_H4096 T=64: one-shot 2.96 us
+    {2, 3, 512, 2048, 1, 1, 3, 1, 2, 2},  // R3_fp16_H4096 T=2048: one-shot 18.012 us cold
+    {2, 3, 512, 2147483647, 1, 1, 3, 1, 1, 4},  // R3_fp16_H4096 T=8192: one-shot 63.392 us cold
+    {2, 4, 1024, 1, 1, 1, 4, 1, 8, 0},  // R4_fp16_H8192 T=1: one-shot 3.184 us
+    {2, 4, 1024, 64, 1, 2, 0, 0, 1, 0},  // R4_fp16_H8192 T=64: one-shot 3.389 us
+    {2, 4, 1024, 1024, 1, 4, 3, 0, 2, 0},  // R4_fp16_H8192 T=1024: one-shot 20.877 us cold
+    {2, 4, 1024, 4096, 1, 4, 3, 1, 1, 4},  // R4_fp16_H8192 T=4096: one-shot 71.029 us cold
+    {2, 4, 1024, 2147483647, 1, 4, 3, 1, 2, 2},  // R4_fp16_H8192 T=8192: one-shot 136.581 us cold
+    {2, 8, 512, 1, 1, 1, 0, 1, 1, 0},  // R8_bf16_H4096 T=1: one-shot 2.909 us
+    {2, 8, 512, 64, 1, 1, 0, 1, 1, 0},  // R8_bf16_H4096 T=64: one-shot 3.101 us
+    {2, 8, 512, 1024, 1, 4, 1, 0, 1, 0},  // R8_bf16_H4096 T=1024: one-shot 16.744 us cold
+    {2, 8, 512, 4096, 1, 1, 3, 1, 1, 2},  // R8_bf16_H4096 T=4096: one-shot 55.578 us cold
+    {2, 8, 512, 2147483647, 1, 1, 3, 1, 1, 2},  // R8_bf16_H4096 T=8192: one-shot 106.717 us cold
+    {2, 8, 1024, 1, 1, 1, 4, 1, 8, 0},  // R8_bf16_H8192 T=1: one-shot 3.206 us
+    {2, 8, 1024, 8, 1, 1, 4, 1, 8, 0},  // R8_bf16_H8192 T=8: one-shot 3.315 us
+    {2, 8, 1024, 32, 1, 1, 4, 1, 4, 0},  // R8_bf16_H8192 T=32: one-shot 3.83 us
+    {2, 8, 1024, 64, 1, 2, 0, 1, 1, 0},  // R8_bf16_H8192 T=64: one-shot 4.019 us
+    {2, 8, 1024, 256, 1, 2, 0, 1, 1, 0},  // R8_bf16_H8192 T=256: one-shot 5.789 us
+    {2, 8, 1024, 512, 1, 4, 1, 0, 1, 0},  // R8_bf16_H8192 T=512: one-shot 17.295 us cold
+    {2, 8, 1024, 1024, 1, 4, 3, 1, 1, 4},  // R8_bf16_H8192 T=1024: one-shot 30.255 us cold
+    {2, 8, 1024, 2048, 1, 2, 3, 1, 1, 2},  // R8_bf16_H8192 T=2048: one-shot 56.376 us cold
+    {2, 8, 1024, 4096, 1, 2, 3, 1, 1, 2},  // R8_bf16_H8192 T=4096: one-shot 106.507 us cold
+    {2, 8, 1024, 2147483647, 1, 2, 3, 1, 1, 2},  // R8_bf16_H8192 T=8192: one-shot 207.824 us cold
+    {2, 16, 1024, 1, 1, 1, 4, 1, 8, 0},  // R16_bf16_H8192 T=1: one-shot 4.934 us
+    {2, 16, 1024, 64, 1, 1, 4, 1, 4, 0},  // R16_bf16_H8192 T=64: one-shot 5.642 us
+    {2, 16, 1024, 2048, 1, 4, 3, 1, 1, 8},  // R16_bf16_H8192 T=2048: one-shot 97.094 us cold
+    {2, 16, 1024, 2147483647, 1, 8, 3, 1, 1, 0},  // R16_bf16_H8192 T=8192: one-shot 365.917 us cold
     {0, 0, 0, 0, 0, 0, 0, 0, 0, 0},  // sentinel
 };
 

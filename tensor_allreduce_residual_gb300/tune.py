@@ -1,6 +1,6 @@
 """Measures the fused path's launch choices and writes the AUTO table.
 
-    python -m tensor_allreduce_residual_gb300.tune sweep results.jsonl [--cases A,B] [--shapes S1,S2] [--tokens T1,T2]
+    python -m tensor_allreduce_residual_gb300.tune sweep results.jsonl [--cases A,B] [--shapes S1,S2] [--tokens T1,T2] [--cold]
     python -m tensor_allreduce_residual_gb300.tune table results.jsonl
     python -m tensor_allreduce_residual_gb300.tune sumsweep sums.jsonl
     python -m tensor_allreduce_residual_gb300.tune sumtable sums.jsonl
@@ -9,9 +9,12 @@
 x when residual_out is written) and the two-shot path on the row shapes of
 the measured workloads, each shape in its own process (the shape override
 AR_ONESHOT_SHAPE is read once per process, by the test build libar_test.so,
-which the children load).  Calls are captured in a CUDA
-graph and replayed, so the numbers are device time without Python launch
-overhead.  `table` keeps the fastest choice per (element size, R, row
+which the children load).  Calls are captured in a CUDA graph and replayed,
+so the numbers are device time without Python launch overhead.  With
+`--cold`, a call whose working set is 64 MB or more is timed instead back to
+back on several input sets that together exceed L2 several times, so that
+every call reads its inputs from DRAM, as a layer's partials would be after
+the rest of a layer's work has passed through L2.  `table` keeps the fastest choice per (element size, R, row
 length, tokens) and rewrites csrc/ar_auto_table.h.  This is the measured
 counterpart of heuristic_min_warp_number / selectImplementation.
 
@@ -46,6 +49,8 @@ CASES = [
 SHAPES = ([f"{v}:{m}:{e}" for v in (1, 2, 4, 8) for m in (0, 1) for e in (0, 1)]
           + [f"{v}:2:{e}" for v in (2, 4) for e in (0, 1)]
           + [f"{v}:3:{e}:{b}" for v in (1, 2, 4, 8) for e in (0, 1) for b in (1, 2)]
+          # the bulk-copy ring with fewer stages than fit (less in flight per SM)
+          + [f"{v}:3:1:{b}:{st}" for v in (1, 2, 4, 8) for b in (1, 2) for st in (2, 4, 8)]
           + [f"{v}:4:1:{c}" for v in (1, 2, 4) for c in (2, 4, 8)])
 
 
@@ -97,7 +102,29 @@ def _graph_time(torch, fn, n=10, reps=5):
     return statistics.median(ts)
 
 
-def _measure(strategy: str, shape: str, out, cases=None, token_filter=None):
+COLD_MIN_BYTES = 64 << 20
+
+
+def _cold_stream_time(torch, fns, rounds=10, reps=3):
+    """Median over `reps` of the mean device time per call of back-to-back calls cycling through `fns`."""
+    s = torch.cuda.current_stream()
+    ts = []
+    for _ in range(reps):
+        for f in fns:
+            f()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(s)
+        for _ in range(rounds):
+            for f in fns:
+                f()
+        b.record(s)
+        torch.cuda.synchronize()
+        ts.append(a.elapsed_time(b) / (rounds * len(fns)))
+    return statistics.median(ts)
+
+
+def _measure(strategy: str, shape: str, out, cases=None, token_filter=None, cold=False):
     """Runs in a child process (AR_ONESHOT_SHAPE already set)."""
     sys.path.insert(0, ROOT)
     import torch
@@ -120,30 +147,37 @@ def _measure(strategy: str, shape: str, out, cases=None, token_filter=None):
                     continue   # no one-shot kernel holds this row
                 if not shape_taken(plan, shape):
                     continue   # the shape does not fit this row: the rule's shape would run instead
-            f = workloads.fused_inputs(R, T, H, dtype, partial_dist=("N", 0.0, 1.0 / R),
-                                       residual_dist=("N", 0.0, 4.0),
-                                       bias_dist=("N", 0.0, 0.02) if has_bias else None,
-                                       weight_dist=("N", 1.0, 0.05), eps=1e-6, device="cuda")
-            o, r = torch.empty_like(f.residual), torch.empty_like(f.residual)
-            ws = torch.empty(ar.ar_workspace_size_rows(R, H, T, ar.dtype_code(f.residual.dtype)),
-                             dtype=torch.uint8, device="cuda")
-            fn = lambda: ar.ar_residual_rmsnorm(f.partials, f.residual, f.weight, f.eps, bias=f.bias,  # noqa: E731
-                                                out=o, residual_out=r, intermediate=ws, strategy=strategy)
+            nbytes = workloads.fused_algorithmic_bytes(R, T, H, dtype, has_bias)
+            timed_cold = cold and nbytes >= COLD_MIN_BYTES
+            nsets = max(2, -(-(400 << 20) // nbytes)) if timed_cold else 1
+            fns = []
+            for k in range(nsets):
+                f = workloads.fused_inputs(R, T, H, dtype, partial_dist=("N", 0.0, 1.0 / R),
+                                           residual_dist=("N", 0.0, 4.0),
+                                           bias_dist=("N", 0.0, 0.02) if has_bias else None,
+                                           weight_dist=("N", 1.0, 0.05), eps=1e-6, seed=k, device="cuda")
+                o, r = torch.empty_like(f.residual), torch.empty_like(f.residual)
+                ws = torch.empty(ar.ar_workspace_size_rows(R, H, T, ar.dtype_code(f.residual.dtype)),
+                                 dtype=torch.uint8, device="cuda")
+                fns.append(lambda f=f, o=o, r=r, ws=ws: ar.ar_residual_rmsnorm(
+                    f.partials, f.residual, f.weight, f.eps, bias=f.bias, out=o, residual_out=r, intermediate=ws,
+                    strategy=strategy))
             try:
-                us = _graph_time(torch, fn) * 1e3
+                us = (_cold_stream_time(torch, fns) if timed_cold else _graph_time(torch, fns[0])) * 1e3
             except ar.ARError:
                 continue
             rec = {"case": name, "R": R, "esize": workloads.ELEM_SIZE[dtype], "units_row": H * workloads.ELEM_SIZE[dtype] // 16,
-                   "T": T, "strategy": strategy, "shape": shape, "us": round(us, 3)}
+                   "T": T, "strategy": strategy, "shape": shape, "us": round(us, 3),
+                   "timing": "cold stream" if timed_cold else "graph replay"}
             if ar.ar_device_status() != ar.AR_OK:
                 raise RuntimeError(f"{strategy} {shape} T={T}: a kernel gave up a bounded wait")
             out.write(json.dumps(rec) + "\n")
             out.flush()
-            del f, o, r, ws
+            del fns
             torch.cuda.empty_cache()
 
 
-def sweep(path: str, cases=None, shapes=None, tokens=None):
+def sweep(path: str, cases=None, shapes=None, tokens=None, cold=False):
     with open(path, "w") as out:
         runs = [("TWOSHOT", "-")] + [("ONESHOT", s) for s in (shapes or SHAPES)]
         for strategy, shape in runs:
@@ -151,7 +185,7 @@ def sweep(path: str, cases=None, shapes=None, tokens=None):
             env.pop("AR_ONESHOT_SHAPE", None)
             if shape != "-":
                 env["AR_ONESHOT_SHAPE"] = shape
-            extra = [",".join(cases or []), ",".join(str(t) for t in (tokens or []))]
+            extra = [",".join(cases or []), ",".join(str(t) for t in (tokens or [])), "cold" if cold else ""]
             res = subprocess.run([sys.executable, "-m", "tensor_allreduce_residual_gb300.tune", "_child",
                                   strategy, shape, *extra], cwd=ROOT, env=env, capture_output=True, text=True)
             if res.returncode != 0:
@@ -177,9 +211,10 @@ def table(path: str):
         items.sort()
         for i, (T, r) in enumerate(items):
             tmax = T if i + 1 < len(items) else 2147483647
+            how = " cold" if r.get("timing") == "cold stream" else ""
             if r["strategy"] == "TWOSHOT":
                 lines.append(f"    {{{esize}, {R}, {units}, {tmax}, 2, 0, 0, 0, 1, 0}},  // {r['case']} T={T}: "
-                             f"two-shot {r['us']} us")
+                             f"two-shot {r['us']} us{how}")
             else:
                 parts = [int(x) for x in r["shape"].split(":")]
                 v, m = parts[0], parts[1]
@@ -187,7 +222,7 @@ def table(path: str):
                 b = parts[3] if len(parts) > 3 else 1
                 st = parts[4] if len(parts) > 4 else 0
                 lines.append(f"    {{{esize}, {R}, {units}, {tmax}, 1, {v}, {m}, {e}, {b}, {st}}},  // {r['case']} T={T}: "
-                             f"one-shot {r['us']} us")
+                             f"one-shot {r['us']} us{how}")
     header = open(TABLE).read()
     start = header.index("static const AutoEntry kAutoTable[] = {")
     end = header.index("};", start)
@@ -287,13 +322,16 @@ if __name__ == "__main__":
     if cmd == "_child":
         cases = [c for c in sys.argv[4].split(",") if c] if len(sys.argv) > 4 else None
         toks = [int(t) for t in sys.argv[5].split(",") if t] if len(sys.argv) > 5 else None
-        _measure(sys.argv[2], sys.argv[3], sys.stdout, cases, toks)
+        _measure(sys.argv[2], sys.argv[3], sys.stdout, cases, toks, cold=len(sys.argv) > 6 and sys.argv[6] == "cold")
     elif cmd == "sweep":
-        # sweep OUT [--cases a,b] [--shapes s1,s2] [--tokens t1,t2]
-        opts = dict(zip(sys.argv[3::2], sys.argv[4::2]))
+        # sweep OUT [--cases a,b] [--shapes s1,s2] [--tokens t1,t2] [--cold]
+        args = sys.argv[3:]
+        cold = "--cold" in args
+        args = [a for a in args if a != "--cold"]
+        opts = dict(zip(args[0::2], args[1::2]))
         sweep(sys.argv[2], cases=[c for c in opts.get("--cases", "").split(",") if c] or None,
               shapes=[c for c in opts.get("--shapes", "").split(",") if c] or None,
-              tokens=[int(t) for t in opts.get("--tokens", "").split(",") if t] or None)
+              tokens=[int(t) for t in opts.get("--tokens", "").split(",") if t] or None, cold=cold)
     elif cmd == "table":
         table(sys.argv[2])
     elif cmd == "sumsweep":
