@@ -290,6 +290,33 @@ def run_ours(args, rank, world, local_rank):
            "us_per_call": round(e2e_ms * 1e3 / args.e2e_steps, 1),
            "note": ("ar_residual_rmsnorm_host on pinned host buffers: inputs copied in and both outputs copied "
                     f"out inside the timed region, {chunk}-row chunks pipelined against the kernels")}
+    # The host link's bound for the same bytes: the step's copies alone (inputs in on one stream, the
+    # outputs' bytes out on another, no kernels), device-timed the same way.
+    s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+
+    def copies_only():
+        s_in.wait_stream(stream)
+        s_out.wait_stream(stream)
+        with torch.cuda.stream(s_in):
+            for h_, d_ in zip(host_parts + [host_res], list(parts) + [resid]):
+                d_.copy_(h_, non_blocking=True)
+        with torch.cuda.stream(s_out):
+            host_out[0].copy_(out, non_blocking=True)
+            host_out[1].copy_(res_out, non_blocking=True)
+        stream.wait_stream(s_in)
+        stream.wait_stream(s_out)
+
+    copies_only()
+    torch.cuda.synchronize()
+    c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    c0.record(stream)
+    for _ in range(3):
+        copies_only()
+    c1.record(stream)
+    torch.cuda.synchronize()
+    copy_us = c0.elapsed_time(c1) * 1e3 / 3
+    e2e["copies_only_us"] = round(copy_us, 1)
+    e2e["frac_of_copies_only"] = round(copy_us / e2e["us_per_call"], 4)
     del host_parts, host_out, staging
 
     extras = None
@@ -409,6 +436,24 @@ def _time_rotate(torch, fns, stream, rounds=10):
     return a.elapsed_time(b) / (rounds * len(fns))
 
 
+def _lamport_l2_bound(ar, torch, R, T, H, s, us):
+    """The Lamport-style call's bound on one GPU.  Its buffer stays in L2 (a ring two grid steps deep), so
+    its DRAM traffic is the fused call's, but every byte of the R partials is written into L2 twice (the
+    push, then the marker that empties it again) besides the two outputs: (2R + 2) T H s bytes of L2
+    writes.  The ceiling for those is measured here with the library's own streaming store kernel (the
+    marker fill, ar_lamport_init, on an L2-resident 64 MB buffer, replayed from a CUDA graph).  The R + 1
+    inputs stream in from DRAM at the same time and share that limit, so the call cannot reach it."""
+    fill = torch.empty(64 << 20, dtype=torch.uint8, device="cuda")
+    w_ms = _time_graph(torch, lambda: ar.ar_lamport_init(fill, torch.bfloat16), n=50, reps=7)
+    del fill
+    w_gbps = (64 << 20) / w_ms / 1e6
+    l2_write = (2 * R + 2) * T * H * s
+    achieved = l2_write / us / 1e3
+    return {"bound": "l2_write", "l2_write_bytes": l2_write, "achieved_GBps": round(achieved, 1),
+            "peak_GBps": round(w_gbps, 1), "frac": round(achieved / w_gbps, 4),
+            "floor_us": round(l2_write / w_gbps / 1e3, 1)}
+
+
 def run_extras(ar, torch, workloads, parts, resid, weight, bias, out, res_out, ws, bytes_call, stream):
     """Secondary numbers: each fixed strategy on the prefill inputs, decode latency, reduce-only bandwidth.
 
@@ -436,7 +481,9 @@ def run_extras(ar, torch, workloads, parts, resid, weight, bias, out, res_out, w
     ex["prefill_LAMPORT"] = {"us_per_call": round(ms * 1e3, 2), "GBps": round(bytes_call / ms / 1e6, 1),
                              "frac_of_peak": round(bytes_call / ms / 1e6 / peak0, 4),
                              "buffer_bytes": lam.numel(),
-                             "over_oneshot": round(ms * 1e3 / ex["prefill_ONESHOT"]["us_per_call"], 3)}
+                             "over_oneshot": round(ms * 1e3 / ex["prefill_ONESHOT"]["us_per_call"], 3),
+                             "l2_bound": _lamport_l2_bound(ar, torch, len(parts), T0, H0, resid.element_size(),
+                                                           ms * 1e3)}
     del lam
     # The unfused route (the pages' "all-reduce, then norm"): ar_sum into a
     # temporary, then the residual + bias + norm call with that sum as its one

@@ -369,6 +369,11 @@ k_fused_lamport(const FusedArgs a, uint4* lam_buffer, const int tpr, const int c
     const long long ring_groups_rows =
         split ? static_cast<long long>(ring_steps) * G / csize : static_cast<long long>(ring_steps) * G * rows;
     const int ring_rows = static_cast<int>(min(static_cast<long long>(min(a.tokens, slot_rows)), ring_groups_rows));
+    // Progress is published only when some ring row is used twice in this
+    // call: otherwise no push ever waits for it, and the barrier and the
+    // release store (which waits for the block's stores to complete) would
+    // only lengthen a short call.
+    const bool ring_reused = ring_rows < a.tokens;
     // The buffer: the blocks' progress words, then the R slots, then the
     // exchange area.
     unsigned long long* progress = reinterpret_cast<unsigned long long*>(lam);
@@ -435,9 +440,11 @@ k_fused_lamport(const FusedArgs a, uint4* lam_buffer, const int tpr, const int c
         }
         push_step(step);
         if (!do_reduce) {
-            __syncthreads();
-            if (threadIdx.x == 0)
-                lamport_publish(progress + b, (static_cast<unsigned long long>(epoch) << 32) | step);
+            if (ring_reused) {
+                __syncthreads();
+                if (threadIdx.x == 0)
+                    lamport_publish(progress + b, (static_cast<unsigned long long>(epoch) << 32) | step);
+            }
             continue;
         }
 
@@ -501,10 +508,15 @@ k_fused_lamport(const FusedArgs a, uint4* lam_buffer, const int tpr, const int c
         }
         // Every thread of the block has taken its vectors of this step and
         // written the marker back: publish the step (the release covers the
-        // whole block's stores through the barrier before it).
-        __syncthreads();
-        if (threadIdx.x == 0)
-            lamport_publish(progress + b, (static_cast<unsigned long long>(epoch) << 32) | step);
+        // whole block's stores through the barrier before it).  Without it
+        // the scratch stays safe: red and tot_s are double-buffered, and a
+        // thread cannot reach the step after next before every thread has
+        // passed the next step's barriers.
+        if (ring_reused) {
+            __syncthreads();
+            if (threadIdx.x == 0)
+                lamport_publish(progress + b, (static_cast<unsigned long long>(epoch) << 32) | step);
+        }
     }
 }
 
@@ -574,6 +586,7 @@ k_fused_lamport_ws(const FusedArgs a, uint4* lam_buffer, const int tpr, const in
     const uint64_t slot_units = static_cast<uint64_t>(slot_rows) * a.units_row;
     const int ring_rows =
         static_cast<int>(min(static_cast<long long>(min(a.tokens, slot_rows)), static_cast<long long>(ring_steps) * G * rows));
+    const bool ring_reused = ring_rows < a.tokens;  // publish progress only then (see k_fused_lamport)
     unsigned long long* progress = reinterpret_cast<unsigned long long*>(lam);
     lam += kLamportProgressBytes / sizeof(uint4);
     const int b = static_cast<int>(blockIdx.x);
@@ -699,9 +712,11 @@ k_fused_lamport_ws(const FusedArgs a, uint4* lam_buffer, const int tpr, const in
         }
         // Every reduce thread has taken its vectors of this step and written
         // the marker back: publish the step.
-        named_sync(1, half);
-        if (t == 0)
-            lamport_publish(progress + b, (static_cast<unsigned long long>(epoch) << 32) | step);
+        if (ring_reused) {
+            named_sync(1, half);
+            if (t == 0)
+                lamport_publish(progress + b, (static_cast<unsigned long long>(epoch) << 32) | step);
+        }
     }
 }
 
