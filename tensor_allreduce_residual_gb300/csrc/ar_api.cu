@@ -442,10 +442,15 @@ int lamport_split_rule(int tokens, int R, int units_row)
 
 // Rows not split, at least this many: separate push and reduce warps
 // (k_fused_lamport_ws), when the reduce side has at most 256 threads of at
-// most 4 vectors each.
-// Measured at R=8 bf16 H=8192: 498-532 us against 569-570 us at 8192
-// rows, 136 against 148 us at 2048, 74-77 against 80 us at 1024, but 25
-// against 19 us at 256.
+// most 4 vectors each, or at most 512 threads of at most 2; two vectors a
+// thread first where that makes the reduce side more than 256 threads
+// (blocks of up to 1024 threads at 64 registers: twice the warps, half the
+// dependent take rounds a step).
+// Measured at R=8 bf16 H=8192, one role / split roles with 4 vectors (512
+// threads) / split roles with 2 vectors (1024 threads): 569-571 / 507-532 /
+// 467-469 us at 8192 rows, 147-148 / 134-137 / 124.4-124.6 us at 2048,
+// 80 / 74-77 / 69.2-69.4 us at 1024; at 256 rows one role is fastest
+// (18.7 against 25.1 and 22.3 us).
 constexpr int kLamportRolesMinTokens = 1024;
 
 // Ring depth of the Lamport buffer, in grid steps.  Deeper rings measured
@@ -460,7 +465,7 @@ bool lamport_shape(int units_row, int tokens, int lanes, int R, OneShotShape* sh
         if (!(oneshot_shape(units_row, vpt, lanes, true, ar::kRegisters, R, sh) &&
               sh->tpr * sh->rows <= ar::lamport_max_threads(vpt * lanes)))
             return false;
-        const bool roles_fit = sh->tpr * sh->rows <= 256 && vpt <= 4;
+        const bool roles_fit = (sh->tpr * sh->rows <= 256 && vpt <= 4) || (sh->tpr * sh->rows <= 512 && vpt <= 2);
         sh->roles = roles_fit && (ov.vpt > 0 ? ov.early : tokens >= kLamportRolesMinTokens) ? 1 : 0;
         sh->stages = ov.vpt > 0 && ov.max_stages >= 2 && ov.max_stages <= ar::kLamportMaxRingSteps
                          ? ov.max_stages
@@ -484,6 +489,8 @@ bool lamport_shape(int units_row, int tokens, int lanes, int R, OneShotShape* sh
         for (int vpt = 1; vpt <= ar::kMaxVPTVec; vpt <<= 1)
             if (fits_split(vpt, c))
                 return true;
+    if (tokens >= kLamportRolesMinTokens && fits(2) && sh->roles && sh->tpr * sh->rows > 256)
+        return true;
     for (int vpt = rule_vpt(units_row, tokens, lanes, true); vpt <= ar::kMaxVPTVec; vpt <<= 1)
         if (fits(vpt))
             return true;

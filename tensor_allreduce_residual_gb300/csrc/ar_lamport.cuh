@@ -146,30 +146,58 @@ __device__ __forceinline__ uint4 lamport_poll(const uint4* p, uint4 v, bool& gav
 }
 
 // x = slot 0 + ... + slot R-1 of vector i in fp32, rank order, each read
-// once it has arrived and then emptied again.  All R first reads are issued
-// before any is checked, so R loads are in flight at once.
-template <typename T, int R_CT>
+// once it has arrived and then emptied again.  The first reads of RG ranks
+// (all R by default) are issued before any is checked, so RG loads are in
+// flight at once; fewer keep fewer registers.
+template <typename T, int R_CT, int RG = R_CT>
 __device__ __forceinline__ void lamport_take(uint4* lam, uint64_t slot_units, int R, uint64_t i, float* x,
                                              bool& gave_up)
 {
     constexpr int L = Lanes<T>::V;
     if constexpr (R_CT > 0) {
-        uint4 v[R_CT];
+        static_assert(RG > 0 && R_CT % RG == 0, "whole groups of ranks");
+        if constexpr (RG == R_CT) {
+            uint4 v[R_CT];
 #pragma unroll
-        for (int r = 0; r < R_CT; ++r)
-            v[r] = ld_relaxed16(lam + r * slot_units + i);
+            for (int r = 0; r < R_CT; ++r)
+                v[r] = ld_relaxed16(lam + r * slot_units + i);
 #pragma unroll
-        for (int r = 0; r < R_CT; ++r)
-            v[r] = lamport_poll<T>(lam + r * slot_units + i, v[r], gave_up);
+            for (int r = 0; r < R_CT; ++r)
+                v[r] = lamport_poll<T>(lam + r * slot_units + i, v[r], gave_up);
 #pragma unroll
-        for (int r = 0; r < R_CT; ++r)
-            st_relaxed16(lam + r * slot_units + i, lamport_empty<T>());
-        Lanes<T>::unpack(v[0], x);
+            for (int r = 0; r < R_CT; ++r)
+                st_relaxed16(lam + r * slot_units + i, lamport_empty<T>());
+            Lanes<T>::unpack(v[0], x);
 #pragma unroll
-        for (int r = 1; r < R_CT; ++r) {
-            float t[L];
-            Lanes<T>::unpack(v[r], t);
-            add_lanes<L>(x, t);
+            for (int r = 1; r < R_CT; ++r) {
+                float t[L];
+                Lanes<T>::unpack(v[r], t);
+                add_lanes<L>(x, t);
+            }
+            return;
+        }
+#pragma unroll
+        for (int r0 = 0; r0 < R_CT; r0 += RG) {
+            uint4 v[RG];
+#pragma unroll
+            for (int r = 0; r < RG; ++r)
+                v[r] = ld_relaxed16(lam + (r0 + r) * slot_units + i);
+#pragma unroll
+            for (int r = 0; r < RG; ++r)
+                v[r] = lamport_poll<T>(lam + (r0 + r) * slot_units + i, v[r], gave_up);
+#pragma unroll
+            for (int r = 0; r < RG; ++r)
+                st_relaxed16(lam + (r0 + r) * slot_units + i, lamport_empty<T>());
+#pragma unroll
+            for (int r = 0; r < RG; ++r) {
+                if (r0 + r == 0) {
+                    Lanes<T>::unpack(v[r], x);
+                } else {
+                    float t[L];
+                    Lanes<T>::unpack(v[r], t);
+                    add_lanes<L>(x, t);
+                }
+            }
         }
     } else {
         for (int r = 0; r < R; ++r) {
@@ -562,13 +590,17 @@ __device__ __forceinline__ float row_sum_named(float v, int tpr, float* red, int
 // of later steps overlap the polls and the row reductions of earlier ones.
 // The push warps move two vectors of every rank per round (2 R loads in
 // flight a thread).  Barriers: id 1 among the reduce warps, id 2 among the
-// push warps; nothing after the split waits on the whole block.  Blocks of
-// at most 512 threads, VPT at most 4 (more would not fit 128 registers).
-template <typename T, int R_CT, int VPT>
-__global__ void __launch_bounds__(512, 1)
+// push warps; nothing after the split waits on the whole block.  MAXT is
+// the largest block: 512 threads with VPT at most 4 (more would not fit 128
+// registers), or 1024 threads with VPT at most 2 (64 registers), where the
+// push warps move one vector of every rank per round.
+template <typename T, int R_CT, int VPT, int MAXT>
+__global__ void __launch_bounds__(MAXT, 1)
 k_fused_lamport_ws(const FusedArgs a, uint4* lam_buffer, const int tpr, const int skip_rank, const int slot_rows,
                    const uint32_t epoch, const int ring_steps)
 {
+    static_assert(MAXT == 512 || (MAXT == 1024 && VPT <= 2), "block and registers");
+    constexpr int PV = MAXT > 512 ? 1 : 2;  // vectors of every rank a push thread moves per round
     pdl_enter();
     using U = Unit<T, true>;
     constexpr int L = U::L;
@@ -611,11 +643,11 @@ k_fused_lamport_ws(const FusedArgs a, uint4* lam_buffer, const int tpr, const in
             }
             if constexpr (R_CT > 0) {
 #pragma unroll
-                for (int k = 0; k < VPT; k += 2) {
-                    uint4 v[2][R_CT];
-                    bool ok[2];
+                for (int k = 0; k < VPT; k += PV) {
+                    uint4 v[PV][R_CT];
+                    bool ok[PV];
 #pragma unroll
-                    for (int h = 0; h < 2; ++h) {
+                    for (int h = 0; h < PV; ++h) {
                         const int j = lane + (k + h) * tpr;
                         ok[h] = k + h < VPT && p_ok && j < a.units_row;
                         if (ok[h]) {
@@ -625,7 +657,7 @@ k_fused_lamport_ws(const FusedArgs a, uint4* lam_buffer, const int tpr, const in
                         }
                     }
 #pragma unroll
-                    for (int h = 0; h < 2; ++h) {
+                    for (int h = 0; h < PV; ++h) {
                         const int j = lane + (k + h) * tpr;
                         if (ok[h]) {
 #pragma unroll
@@ -675,7 +707,8 @@ k_fused_lamport_ws(const FusedArgs a, uint4* lam_buffer, const int tpr, const in
                 for (int l = 0; l < L; ++l)
                     x[k][l] = 0.0f;
                 if (row_ok && j < a.units_row)
-                    lamport_take<T, R_CT>(lam, slot_units, R, row_ring + j, x[k], gave_up);
+                    lamport_take<T, R_CT, (MAXT > 512 && R_CT > 4) ? 4 : R_CT>(lam, slot_units, R, row_ring + j,
+                                                                              x[k], gave_up);
             }
 #pragma unroll
             for (int k = 0; k < VPT; ++k) {
@@ -688,7 +721,8 @@ k_fused_lamport_ws(const FusedArgs a, uint4* lam_buffer, const int tpr, const in
                     }
                     U::to_float(rv[k], tv);
                     add_lanes<L>(x[k], tv);
-                    wv[k] = U::load_cached(a.weight, j);
+                    if constexpr (MAXT <= 512)
+                        wv[k] = U::load_cached(a.weight, j);
                     U::store(a.residual_out, row_off + j, x[k]);
 #pragma unroll
                     for (int l = 0; l < L; ++l)
@@ -702,6 +736,8 @@ k_fused_lamport_ws(const FusedArgs a, uint4* lam_buffer, const int tpr, const in
                 const int j = lane + k * tpr;
                 if (row_ok && j < a.units_row) {
                     float w[L], y[L];
+                    if constexpr (MAXT > 512)  // loaded late: 64 registers a thread
+                        wv[k] = U::load_cached(a.weight, j);
                     U::to_float(wv[k], w);
 #pragma unroll
                     for (int l = 0; l < L; ++l)

@@ -360,12 +360,16 @@ template <typename T, int R_CT, int VPT>
 static cudaError_t run_lamport_ws(const FusedArgs& a, void* lam, OneShotShape sh, int skip_rank, uint32_t epoch,
                                   cudaStream_t s)
 {
-    auto kernel = k_fused_lamport_ws<T, R_CT, VPT>;
     const int threads = 2 * sh.tpr * sh.rows;
+    auto kernel = k_fused_lamport_ws<T, R_CT, VPT, 512>;
+    if constexpr (VPT <= 2) {
+        if (threads > 512)
+            kernel = k_fused_lamport_ws<T, R_CT, VPT, 1024>;
+    }
     const int ring_steps = sh.stages;
     if (ring_steps < 2 || ring_steps > kLamportMaxRingSteps)
         return cudaErrorInvalidValue;
-    if (sh.mode == kCluster || threads > 512)
+    if (sh.mode == kCluster || threads > (VPT <= 2 ? 1024 : 512))
         return cudaErrorInvalidConfiguration;
     int dev = 0, sms = 0, per_sm = 0;
     cudaError_t e = cudaGetDevice(&dev);

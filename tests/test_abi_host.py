@@ -406,11 +406,12 @@ def test_lamport_buffer_size_support_and_init(L):
                 (2, 64, 1, 9)]:
         assert L.ar_lamport_buffer_size(*bad) == 0
     w = ctypes.c_int(-1)
-    # up to 8 rows of many vectors: a row split over 4 blocks; else one block a row, 16 warps up to 512 rows
+    # up to 8 rows of many vectors: a row split over 4 blocks; else one block a row, 16 warps up to 512 rows;
+    # from 1024 rows separate push and reduce warps, the reduce side 16 warps a row of two vectors a thread
     assert L.ar_lamport_supported(8, 8192, 1, ar.AR_BF16, ctypes.byref(w)) == ar.AR_OK and w.value == 32
     assert L.ar_lamport_supported(2, 4096, 32, ar.AR_FP16, ctypes.byref(w)) == ar.AR_OK and w.value == 16
     assert L.ar_lamport_supported(8, 8192, 256, ar.AR_BF16, ctypes.byref(w)) == ar.AR_OK and w.value == 16
-    assert L.ar_lamport_supported(8, 8192, 4096, ar.AR_BF16, ctypes.byref(w)) == ar.AR_OK and w.value == 8
+    assert L.ar_lamport_supported(8, 8192, 4096, ar.AR_BF16, ctypes.byref(w)) == ar.AR_OK and w.value == 16
     assert L.ar_lamport_supported(2, 16384, 1, ar.AR_BF16, ctypes.byref(w)) == ar.AR_OK and w.value == 8
     assert L.ar_lamport_supported(2, 16384, 100, ar.AR_BF16, ctypes.byref(w)) == ar.AR_OK and w.value == 8
     assert L.ar_lamport_supported(2, 64, 4, ar.AR_FP32, ctypes.byref(w)) == ar.AR_OK and w.value == 1
