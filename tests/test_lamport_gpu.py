@@ -96,6 +96,10 @@ def _inputs(R, T, H, dtype, bias=True, seed=0):
     (5, 300, 768, "fp16", True),       # rows in groups of several per block, blocks striding
     (4, 3000, 1024, "bf16", True),     # more rows than the ring holds: ring rows reused within the call
     (2, 20000, 64, "fp32", True),      # the same with 8 rows a group
+    # separate push and reduce warps in blocks of 1024 threads (two vectors a thread, 512 a row):
+    (3, 1100, 8192, "fp16", True),     # runtime rank count
+    (4, 1500, 4096, "fp32", True),     # fp32 rows
+    (8, 1200, 6000, "bf16", False),    # ragged row: 750 vectors over 512 threads
 ])
 def test_parity_with_oracle(R, T, H, dtype, bias):
     inp = _inputs(R, T, H, dtype, bias, seed=R * 100 + T)
