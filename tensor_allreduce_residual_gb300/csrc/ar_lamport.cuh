@@ -588,12 +588,15 @@ __device__ __forceinline__ float row_sum_named(float v, int tpr, float* red, int
 // push into a reused ring row waits for its reducer's progress word), so a
 // reduce finds its neighbour's data already pushed, and the partials' loads
 // of later steps overlap the polls and the row reductions of earlier ones.
-// The push warps move two vectors of every rank per round (2 R loads in
-// flight a thread).  Barriers: id 1 among the reduce warps, id 2 among the
-// push warps; nothing after the split waits on the whole block.  MAXT is
-// the largest block: 512 threads with VPT at most 4 (more would not fit 128
-// registers), or 1024 threads with VPT at most 2 (64 registers), where the
-// push warps move one vector of every rank per round.
+// Barriers: id 1 among the reduce warps, id 2 among the push warps; nothing
+// after the split waits on the whole block.  MAXT is the largest block:
+//   512 threads, VPT at most 4 (more would not fit 128 registers): the push
+//     warps move two vectors of every rank per round (2R loads in flight a
+//     thread), and a reduce thread takes all R ranks of a vector at once;
+//   1024 threads, VPT at most 2 (64 registers): twice the warps; the push
+//     warps move one vector of every rank per round, a reduce thread takes
+//     the ranks of a vector four at a time (when R > 4) and loads its
+//     weight after the row sum.
 template <typename T, int R_CT, int VPT, int MAXT>
 __global__ void __launch_bounds__(MAXT, 1)
 k_fused_lamport_ws(const FusedArgs a, uint4* lam_buffer, const int tpr, const int skip_rank, const int slot_rows,
