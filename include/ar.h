@@ -569,7 +569,8 @@ int ar_comm_destroy(ar_comm* comm);
 /*
  * ar_allreduce_peer -- out = sum over the ranks of `input`, n elements of
  * dtype, on every rank.  input and out: this rank's device memory, 16-byte
- * aligned; out may equal input.  n * element size <= max_bytes.
+ * aligned; out may equal input.  n * element size <= max_bytes.  The
+ * current device must be the one the communicator was created on.
  *   strategy  AR_ONESHOT: every rank reads all n elements of every peer.
  *             AR_TWOSHOT: rank r reduces slice r of every peer (the
  *             reduce-scatter) and gathers the other slices from their
@@ -577,8 +578,12 @@ int ar_comm_destroy(ar_comm* comm);
  *             or under 1 MiB, two-shot beyond (a size rule, not measured).
  *             Values are bit-identical across strategies.
  * Asynchronous on `stream`; stream-ordered with the calls before it.
- * Errors: AR_ERR_INVALID_ARG, AR_ERR_UNSUPPORTED (dtype, strategy, or a
- * misaligned pointer), AR_ERR_WORKSPACE (n beyond max_bytes), AR_ERR_CUDA.
+ * After a wait gave up (AR_ERR_TIMEOUT from ar_device_status), the ranks'
+ * barrier words no longer agree on the calls made: destroy the
+ * communicator on every rank and create it again before the next call.
+ * Errors: AR_ERR_INVALID_ARG (also: another current device),
+ * AR_ERR_UNSUPPORTED (dtype, strategy, or a misaligned pointer),
+ * AR_ERR_WORKSPACE (n beyond max_bytes), AR_ERR_CUDA.
  */
 int ar_allreduce_peer(ar_comm* comm, const void* input, void* out, size_t n, int dtype, int strategy,
                       ar_stream_t stream);

@@ -380,6 +380,11 @@ int ar_allreduce_peer(ar_comm* comm, const void* input, void* out, size_t n, int
 {
     if (comm == nullptr)
         return AR_ERR_INVALID_ARG;
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess)
+        return AR_ERR_CUDA;
+    if (dev != comm->device)  // its peers' mappings belong to that device
+        return AR_ERR_INVALID_ARG;
     const int esize = peer_esize(dtype);
     if (esize == 0)
         return AR_ERR_UNSUPPORTED;
