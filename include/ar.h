@@ -468,12 +468,14 @@ int ar_lamport_init(void* buffer, size_t bytes, int dtype, ar_stream_t stream);
  * Lamport call can take this shape, with *warps_per_token (nullable) set to
  * the warps that reduce one row (the heuristic_min_warp_number analogue).
  * The shape must have hidden a multiple of 16 / element size and a row that
- * fits: one block of at most 512 threads (256 when a thread holds more than
- * 16 values) takes a row, up to 8 16-byte vectors a thread, except that up
- * to 8 tokens whose R partials hold at least 8192 vectors a row are split
- * over 4 such blocks.  So rows of up to 2048 vectors (16384 fp16 / bf16,
- * 8192 fp32 elements) are always taken, and up to 4 times longer ones in
- * that split case.
+ * fits: at most 512 threads (256 when a thread holds more than 16 values)
+ * reduce a row, up to 8 16-byte vectors a thread, except that up to 8
+ * tokens whose R partials hold at least 8192 vectors a row are split over 4
+ * such blocks.  So rows of up to 2048 vectors (16384 fp16 / bf16, 8192 fp32
+ * elements) are always taken, and up to 4 times longer ones in that split
+ * case.  From 1024 tokens, where a row's reducing threads number at most
+ * 512 with at most 4 vectors each, the same block also holds as many
+ * threads again that push the partials (blocks of up to 1024 threads).
  * Host-side only: launches nothing.  Pointer alignment is checked by the
  * call itself.
  * Errors: AR_ERR_INVALID_ARG (bad R, hidden or tokens),
