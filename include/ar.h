@@ -474,8 +474,9 @@ int ar_lamport_init(void* buffer, size_t bytes, int dtype, ar_stream_t stream);
  * such blocks.  So rows of up to 2048 vectors (16384 fp16 / bf16, 8192 fp32
  * elements) are always taken, and up to 4 times longer ones in that split
  * case.  From 1024 tokens, where a row's reducing threads number at most
- * 512 with at most 4 vectors each, the same block also holds as many
- * threads again that push the partials (blocks of up to 1024 threads).
+ * 256 with at most 4 vectors each, or at most 512 with at most 2, the same
+ * block also holds as many threads again that push the partials (blocks of
+ * up to 1024 threads).
  * Host-side only: launches nothing.  Pointer alignment is checked by the
  * call itself.
  * Errors: AR_ERR_INVALID_ARG (bad R, hidden or tokens),
