@@ -528,10 +528,13 @@ def run_extras(ar, torch, workloads, parts, resid, weight, bias, out, res_out, w
     # Cold stream: back to back on input sets that together exceed L2 several
     # times, so every call's inputs come from DRAM.  Warm: back-to-back calls
     # on the same inputs.  copy_us_cold: a plain device copy of the same
-    # number of bytes timed like `cold`; read_same_bytes_us_cold: a read-only
-    # pass (a sum) over as many bytes as the call reads (its 9 inputs), timed
-    # the same way -- the floors that this way of timing sets at each size
-    # (an isolated launch between events costs about 4 us here by itself).
+    # number of bytes timed like `cold` (half of them read; after the flush
+    # L2 holds only clean lines, so the copy's writes, like the call's, stay
+    # in the write-back L2 within the interval and its time is mostly that of
+    # its reads); read_same_bytes_us_cold: a read-only pass (a sum) over as
+    # many bytes as the call reads (its 9 inputs), timed the same way -- the
+    # floor this way of timing sets for the call's reads at each size (an
+    # isolated launch between events costs about 4 us here by itself).
     peak, _ = measured_peaks()
     curve = {}
     for T in (512, 1024, 2048, 4096):
