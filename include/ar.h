@@ -208,12 +208,14 @@ size_t ar_host_staging_size(int R, int hidden, int chunk_tokens, int dtype);
  * ar_residual_rmsnorm_host -- ar_residual_rmsnorm on tensors in HOST memory
  * (partials, bias, residual, weight, out, residual_out: same shapes and
  * meaning), for data that is not resident on the device.  The call copies
- * the rows in chunks of chunk_tokens rows into `staging` (device memory of
- * at least ar_host_staging_size(R, hidden, chunk_tokens, dtype) bytes,
- * 256-byte aligned, owned by the caller), runs the fused kernels on each
- * chunk on `stream`, and copies the outputs back, with the copies of chunk
- * i+1 and i-1 overlapping the kernels of chunk i (two staging buffers, two
- * copy streams).  No pages' counterpart: the plugin of "All Reduce Plugin"
+ * the rows in chunks of chunk_tokens rows (the last chunk_tokens rows in
+ * shrinking pieces, halves until at most 128 rows are left, so that little
+ * is left to do after the last copy in) into `staging` (device memory of at least
+ * ar_host_staging_size(R, hidden, chunk_tokens, dtype) bytes, 256-byte
+ * aligned, owned by the caller), runs the fused kernels on each chunk on
+ * `stream`, and copies the outputs back, with the copies of chunk i+1 and
+ * i-1 overlapping the kernels of chunk i (two staging buffers, two copy
+ * streams).  No pages' counterpart: the plugin of "All Reduce Plugin"
  * works on device tensors only.
  *
  * Asynchronous like every call here: it returns once everything is queued.

@@ -8,18 +8,25 @@
 //   caller's stream  ar_residual_rmsnorm on the staged chunk
 //   copy-out stream  out and residual_out chunks, device -> host
 // so chunk i+1 is copied in while chunk i is computed and chunk i-1 copied
-// out.  Events order each buffer's reuse after its previous copy-out.  Work
+// out.  The last chunk_tokens rows (or fewer) go in shrinking pieces, halves
+// until at most 2 x kMinTailRows rows are left, so that what runs after the
+// last copy in (the drain: a piece's kernel and its copy out) is a small
+// piece's, not a whole chunk's.  Events order each buffer's reuse after its
+// previous copy-out.  Work
 // queued on the caller's stream before the call is ordered before every copy
 // of the call, and work queued after the call sees the outputs in host memory.
 #include <cuda_runtime.h>
 
 #include <mutex>
+#include <utility>
+#include <vector>
 
 #include "ar.h"
 
 namespace {
 
 constexpr int kBuffers = 2;      // staging buffers in the ring
+constexpr int kMinTailRows = 64; // pieces of the shrinking tail stop halving at 2x this
 constexpr int kMaxDevices = 64;
 
 size_t round256(size_t b) { return (b + 255) / 256 * 256; }
@@ -157,11 +164,24 @@ extern "C" int ar_residual_rmsnorm_host(const void* const* partials, int R, cons
     AR_TRY(cudaEventRecord(P->consts, P->copy_in));
     AR_TRY(cudaStreamWaitEvent(cs, P->consts, 0));
 
-    const int nchunks = (tokens + chunk_tokens - 1) / chunk_tokens;
+    // (first row, rows) of every piece: whole chunks, then the shrinking tail.
+    std::vector<std::pair<int, int>> pieces;
+    int next = 0;
+    while (tokens - next > chunk_tokens) {
+        pieces.emplace_back(next, chunk_tokens);
+        next += chunk_tokens;
+    }
+    for (int rem = tokens - next; rem > 0;) {
+        const int p = rem > 2 * kMinTailRows ? (rem + 1) / 2 : rem;
+        pieces.emplace_back(next, p);
+        next += p;
+        rem -= p;
+    }
+    const int nchunks = static_cast<int>(pieces.size());
     for (int i = 0; i < nchunks; ++i) {
         const int b = i % kBuffers;
-        const int t0 = i * chunk_tokens;
-        const int rows = tokens - t0 < chunk_tokens ? tokens - t0 : chunk_tokens;
+        const int t0 = pieces[i].first;
+        const int rows = pieces[i].second;
         const size_t off = static_cast<size_t>(t0) * row;
         const size_t bytes = static_cast<size_t>(rows) * row;
         char* buf = base + b * L.buffer;

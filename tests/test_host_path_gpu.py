@@ -1,8 +1,8 @@
 """ar_residual_rmsnorm_host: the fused call on host tensors, copies pipelined
 through device staging.  Its outputs must match the oracle like the device
 call's, residual_out bit for bit with the device call, for row counts that
-split into several chunks with a ragged last one, a single chunk, and chunk
-sizes of one row."""
+split into several chunks with a ragged last one, a single chunk, chunk
+sizes of one row, and a last chunk cut into shrinking pieces."""
 import pytest
 import torch
 
@@ -73,14 +73,25 @@ def test_host_path_repeated_calls_share_nothing_stale():
         _check(inp, *_run_host(inp, 5))
 
 
+def test_host_path_shrinking_tail():
+    """The last chunk's rows go in halves until at most 128 are left: 1000 rows in chunks of 700 are pieces
+    of 700, 150, 75 and 75 rows (ragged, and more pieces than staging buffers)."""
+    inp = workloads.fused_inputs(4, 1000, 1024, "bf16", partial_dist=("N", 0.0, 0.25), residual_dist=("N", 0.0, 4.0),
+                                 bias_dist=("N", 0.0, 0.02), weight_dist=("N", 1.0, 0.05), eps=1e-6, seed=21)
+    _check(inp, *_run_host(inp, 700))
+
+
 def test_host_path_full_prefill_sampled_rows():
     """The end-to-end configuration bench.py times: 8192 x 8192 R=8 bf16 with bias on pinned host buffers,
-    512-row chunks, AUTO; sampled rows against the oracle, and residual_out bit for bit with the device call."""
+    4096-row chunks (one whole chunk, then pieces of 2048, 1024, 512, 256, 128 and 128 rows), AUTO;
+    sampled rows, the pieces' first and last among them, against the oracle, and residual_out bit for bit
+    with the device call."""
     inp = workloads.tp_prefill(seed=3)
     T, H = inp.tokens, inp.hidden
-    out, rout = _run_host(inp, 512)
+    out, rout = _run_host(inp, 4096)
     g = torch.Generator().manual_seed(11)
-    rows = sorted(set([0, 511, 512, 4095, 4096, T - 1] + torch.randint(0, T, (16,), generator=g).tolist()))
+    edges = [0, 4095, 4096, 6143, 6144, 7167, 7168, 7679, 7680, 7935, 7936, 8063, 8064, T - 1]
+    rows = sorted(set(edges + torch.randint(0, T, (16,), generator=g).tolist()))
     ridx = torch.tensor(rows)
     sub = workloads.FusedInputs(inp.R, len(rows), H, inp.dtype, inp.eps,
                                 [p[ridx].contiguous() for p in inp.partials], inp.residual[ridx].contiguous(),
