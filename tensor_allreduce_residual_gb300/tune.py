@@ -1,6 +1,6 @@
 """Measures the fused path's launch choices and writes the AUTO table.
 
-    python -m tensor_allreduce_residual_gb300.tune sweep results.jsonl [--cases A,B] [--shapes S1,S2] [--tokens T1,T2] [--cold]
+    python -m tensor_allreduce_residual_gb300.tune sweep results.jsonl [--cases A,B] [--shapes S1,S2] [--tokens T1,T2] [--cold] [--alone]
     python -m tensor_allreduce_residual_gb300.tune table results.jsonl
     python -m tensor_allreduce_residual_gb300.tune sumsweep sums.jsonl
     python -m tensor_allreduce_residual_gb300.tune sumtable sums.jsonl
@@ -14,7 +14,10 @@ so the numbers are device time without Python launch overhead.  With
 `--cold`, a call whose working set is 64 MB or more is timed instead back to
 back on several input sets that together exceed L2 several times, so that
 every call reads its inputs from DRAM, as a layer's partials would be after
-the rest of a layer's work has passed through L2.  `table` keeps the fastest choice per (element size, R, row
+the rest of a layer's work has passed through L2.  With `--alone` as well,
+such a call is also timed alone after an L2 flush (a 256 MB buffer written,
+then another read, a device sleep, one event pair per call, mean of 30),
+recorded as `us_alone`; the table ignores it.  `table` keeps the fastest choice per (element size, R, row
 length, tokens) and rewrites csrc/ar_auto_table.h.  This is the measured
 counterpart of heuristic_min_warp_number / selectImplementation.
 
@@ -124,7 +127,29 @@ def _cold_stream_time(torch, fns, rounds=10, reps=3):
     return statistics.median(ts)
 
 
-def _measure(strategy: str, shape: str, out, cases=None, token_filter=None, cold=False):
+def _alone_time(torch, fn, n=30):
+    """Mean device time of `fn` called alone after an L2 flush (written, then a second buffer read, so
+    that L2 holds clean lines only), with a device sleep covering the host's launch of the call."""
+    flush = (torch.empty(256 << 20, dtype=torch.uint8, device="cuda"),
+             torch.zeros(256 << 20, dtype=torch.uint8, device="cuda"))
+    s = torch.cuda.current_stream()
+    fn()
+    torch.cuda.synchronize()
+    ts = []
+    for _ in range(n):
+        flush[0].zero_()
+        flush[1].amax()
+        torch.cuda._sleep(50000)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(s)
+        fn()
+        b.record(s)
+        torch.cuda.synchronize()
+        ts.append(a.elapsed_time(b))
+    return statistics.mean(ts)
+
+
+def _measure(strategy: str, shape: str, out, cases=None, token_filter=None, cold=False, alone=False):
     """Runs in a child process (AR_ONESHOT_SHAPE already set)."""
     sys.path.insert(0, ROOT)
     import torch
@@ -169,6 +194,8 @@ def _measure(strategy: str, shape: str, out, cases=None, token_filter=None, cold
             rec = {"case": name, "R": R, "esize": workloads.ELEM_SIZE[dtype], "units_row": H * workloads.ELEM_SIZE[dtype] // 16,
                    "T": T, "strategy": strategy, "shape": shape, "us": round(us, 3),
                    "timing": "cold stream" if timed_cold else "graph replay"}
+            if alone and timed_cold:
+                rec["us_alone"] = round(_alone_time(torch, fns[0]) * 1e3, 3)
             if ar.ar_device_status() != ar.AR_OK:
                 raise RuntimeError(f"{strategy} {shape} T={T}: a kernel gave up a bounded wait")
             out.write(json.dumps(rec) + "\n")
@@ -177,7 +204,7 @@ def _measure(strategy: str, shape: str, out, cases=None, token_filter=None, cold
             torch.cuda.empty_cache()
 
 
-def sweep(path: str, cases=None, shapes=None, tokens=None, cold=False):
+def sweep(path: str, cases=None, shapes=None, tokens=None, cold=False, alone=False):
     with open(path, "w") as out:
         runs = [("TWOSHOT", "-")] + [("ONESHOT", s) for s in (shapes or SHAPES)]
         for strategy, shape in runs:
@@ -185,7 +212,8 @@ def sweep(path: str, cases=None, shapes=None, tokens=None, cold=False):
             env.pop("AR_ONESHOT_SHAPE", None)
             if shape != "-":
                 env["AR_ONESHOT_SHAPE"] = shape
-            extra = [",".join(cases or []), ",".join(str(t) for t in (tokens or [])), "cold" if cold else ""]
+            extra = [",".join(cases or []), ",".join(str(t) for t in (tokens or [])), "cold" if cold else "",
+                     "alone" if alone else ""]
             res = subprocess.run([sys.executable, "-m", "tensor_allreduce_residual_gb300.tune", "_child",
                                   strategy, shape, *extra], cwd=ROOT, env=env, capture_output=True, text=True)
             if res.returncode != 0:
@@ -322,16 +350,18 @@ if __name__ == "__main__":
     if cmd == "_child":
         cases = [c for c in sys.argv[4].split(",") if c] if len(sys.argv) > 4 else None
         toks = [int(t) for t in sys.argv[5].split(",") if t] if len(sys.argv) > 5 else None
-        _measure(sys.argv[2], sys.argv[3], sys.stdout, cases, toks, cold=len(sys.argv) > 6 and sys.argv[6] == "cold")
+        _measure(sys.argv[2], sys.argv[3], sys.stdout, cases, toks, cold=len(sys.argv) > 6 and sys.argv[6] == "cold",
+                 alone=len(sys.argv) > 7 and sys.argv[7] == "alone")
     elif cmd == "sweep":
-        # sweep OUT [--cases a,b] [--shapes s1,s2] [--tokens t1,t2] [--cold]
+        # sweep OUT [--cases a,b] [--shapes s1,s2] [--tokens t1,t2] [--cold] [--alone]
         args = sys.argv[3:]
         cold = "--cold" in args
-        args = [a for a in args if a != "--cold"]
+        alone = "--alone" in args
+        args = [a for a in args if a not in ("--cold", "--alone")]
         opts = dict(zip(args[0::2], args[1::2]))
         sweep(sys.argv[2], cases=[c for c in opts.get("--cases", "").split(",") if c] or None,
               shapes=[c for c in opts.get("--shapes", "").split(",") if c] or None,
-              tokens=[int(t) for t in opts.get("--tokens", "").split(",") if t] or None, cold=cold)
+              tokens=[int(t) for t in opts.get("--tokens", "").split(",") if t] or None, cold=cold, alone=alone)
     elif cmd == "table":
         table(sys.argv[2])
     elif cmd == "sumsweep":
