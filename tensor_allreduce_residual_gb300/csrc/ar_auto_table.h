@@ -63,7 +63,7 @@ static const AutoEntry kAutoTable[] = {
     {2, 8, 1024, 64, 1, 2, 0, 1, 1, 0},  // R8_bf16_H8192 T=64: one-shot 4.019 us
     {2, 8, 1024, 256, 1, 2, 0, 1, 1, 0},  // R8_bf16_H8192 T=256: one-shot 5.789 us
     {2, 8, 1024, 512, 1, 4, 1, 0, 1, 0},  // R8_bf16_H8192 T=512: one-shot 17.295 us cold
-    {2, 8, 1024, 1024, 1, 4, 3, 1, 1, 4},  // R8_bf16_H8192 T=1024: one-shot 30.255 us cold
+    {2, 8, 1024, 1024, 1, 2, 3, 1, 1, 2},  // R8_bf16_H8192 T=1024: one-shot 29.86 us cold
     {2, 8, 1024, 2048, 1, 2, 3, 1, 1, 2},  // R8_bf16_H8192 T=2048: one-shot 56.376 us cold
     {2, 8, 1024, 4096, 1, 2, 3, 1, 1, 2},  // R8_bf16_H8192 T=4096: one-shot 106.507 us cold
     {2, 8, 1024, 2147483647, 1, 2, 3, 1, 1, 2},  // R8_bf16_H8192 T=8192: one-shot 207.824 us cold
